@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash drafting step on GB300: one JSON line on stdout.
+
+A step is one drafting cycle at a fixed context: the tapped hidden states of
+the R = gamma + 1 newest verified positions are fused (dflash_ctx_fuse) and
+injected into every layer's KV cache (dflash_kv_inject), the drafter drafts
+one block over the N-row context (dflash_draft_block) and the block is
+verified against synthetic target logits (dflash_verify_accept). The context
+length is restored before every step, so every step sees exactly N rows.
+
+Metric: drafted tokens/s (B * gamma per step) and the step time; value is the
+device-timed throughput with inputs resident in HBM, e2e the same through
+host buffers (pinned H2D of the step's inputs, D2H of its outputs).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "qwen3_8b_L5_N2048_B1"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
+    p.add_argument("--cpu-steps", type=int, default=2, help="oracle steps timed for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+class DraftCycle:
+    """Device state of one drafting cycle for a workload (one replica)."""
+
+    def __init__(self, dfl, wl: synth.Workload, device: str):
+        self.dfl, self.wl, self.dev = dfl, wl, device
+        R, B = wl.rows, wl.batch
+        self.cfg = dfl.config_from_workload(wl)
+        self.W = synth.weights(wl, device)
+        self.w = dfl.Weights(self.cfg, self.W, device)
+        prefix = synth.ctx_lengths(wl) - R          # context before the step's injection
+        if (prefix < 0).any():
+            raise ValueError("context shorter than one block")
+        self.prefix = prefix
+        self.ws = dfl.Workspace(self.cfg, max(int(prefix.max()) * B, B * R, 16), device)
+        dt = synth.torch_dtype(wl.dtype)
+        shape = (wl.n_layers, self.cfg.max_batch, wl.n_kv_heads, self.cfg.ctx_capacity, wl.head_dim)
+        self.k_cache = torch.zeros(shape, dtype=dt, device=device)
+        self.v_cache = torch.zeros(shape, dtype=dt, device=device)
+        self.ctx_len = torch.zeros(B, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # prefill of the prefix context (set-up, not timed)
+        tmax = int(prefix.max())
+        taps = synth.taps(wl, B * tmax, "prefill", device).view(B, tmax, -1)
+        h = torch.empty((B, tmax, wl.d_model), dtype=dt, device=device)
+        for b in range(B):
+            dfl.dflash_ctx_fuse(self.cfg, self.w, taps[b, : int(prefix[b])], h[b], self.ws)
+        del taps
+        dfl.dflash_kv_inject(self.cfg, self.w, h, torch.as_tensor(prefix, device=device),
+                             self.ctx_len, self.k_cache, self.v_cache, self.status, self.ws)
+        del h
+        self.ctx0 = self.ctx_len.clone()
+        # per-step inputs
+        self.step_taps = synth.taps(wl, B * R, "step", device)
+        self.h_new = torch.empty((B, R, wl.d_model), dtype=dt, device=device)
+        self.n_new = torch.full((B,), R, dtype=torch.int32, device=device)
+        self.anchor = torch.as_tensor(synth.anchors(wl), device=device)
+        self.target = synth.target_logits(wl, "step", device, torch.float32)
+        self.draft = torch.empty((B, wl.gamma), dtype=torch.int32, device=device)
+        self.tau = torch.empty(B, dtype=torch.int32, device=device)
+        self.committed = torch.empty((B, R), dtype=torch.int32, device=device)
+        self.next_anchor = torch.empty(B, dtype=torch.int32, device=device)
+        self.max_ctx = int(synth.ctx_lengths(wl).max())
+        torch.cuda.synchronize()
+
+    def step(self, trace=None):
+        d, wl = self.dfl, self.wl
+        self.ctx_len.copy_(self.ctx0)
+        d.dflash_ctx_fuse(self.cfg, self.w, self.step_taps, self.h_new.view(-1, wl.d_model), self.ws)
+        d.dflash_kv_inject(self.cfg, self.w, self.h_new, self.n_new, self.ctx_len, self.k_cache,
+                           self.v_cache, self.status, self.ws)
+        d.dflash_draft_block(self.cfg, self.w, self.anchor, self.ctx_len, self.max_ctx, self.k_cache,
+                             self.v_cache, self.draft, self.status, self.ws, trace=trace)
+        d.dflash_verify_accept(self.cfg, self.target, self.draft, self.tau, self.committed,
+                               self.next_anchor, self.ws, trace=trace)
+
+    def launches_per_step(self) -> int:
+        rec = self.dfl.TraceRecorder(256)
+        self.step(trace=rec.struct)
+        torch.cuda.synchronize()
+        return rec.struct.count + 4   # + fusion GEMM, fusion norm, injection GEMM, length advance
+
+
+def time_steps(fn, steps: int, stream) -> float:
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def kernel_roofline(cyc: DraftCycle, peak_gbs: float, reps: int = 5):
+    """Per-kind algorithmic bytes / CUDA-event time over traced steps."""
+    dfl = cyc.dfl
+    rec = dfl.TraceRecorder(512)
+    agg = {}
+    for _ in range(reps):
+        rec.reset()
+        cyc.step(trace=rec.struct)
+        for kind, b, fl, ms in rec.records():
+            a = agg.setdefault(kind, [0.0, 0.0, 0.0, 0])
+            a[0] += b
+            a[1] += fl
+            a[2] += ms
+            a[3] += 1
+    names = {dfl.K_GEMM: "gemm_tc", dfl.K_ATTN: "attention", dfl.K_NORM: "row_kernels",
+             dfl.K_ARGMAX: "argmax", dfl.K_VERIFY: "verify"}
+    out = {}
+    for kind, (b, fl, ms, n) in agg.items():
+        gbs = b / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+        out[names.get(kind, str(kind))] = {
+            "launches_per_step": n // reps, "ms_per_step": ms / reps, "bytes_per_launch": b / n,
+            "achieved_gbs": gbs, "frac_of_hbm": gbs / peak_gbs, "tflops": fl / (ms * 1e-3) / 1e12 if ms > 0 else 0.0}
+    return out
+
+
+class OracleCycle:
+    """The CPU oracle running the same drafting cycle (float64 numpy)."""
+
+    def __init__(self, wl: synth.Workload, W: dict, device: str):
+        from oracle import dflash_ref as ref
+        self.ref, self.wl = ref, wl
+        self.oc = ref.Cfg(wl.n_layers, wl.d_target, wl.n_taps, wl.d_model, wl.n_q_heads,
+                          wl.n_kv_heads, wl.head_dim, wl.d_ffn, wl.vocab, wl.gamma,
+                          wl.mask_token_id, wl.rms_eps, wl.rope_theta)
+        # weights as float64 once (set-up); the embedding stays a CPU tensor (gathered per use)
+        self.W = {k: (v.cpu() if k == "embed" else ref.f64(v)) for k, v in W.items()}
+        R, B = wl.rows, wl.batch
+        prefix = synth.ctx_lengths(wl) - R
+        tmax = int(prefix.max())
+        taps = synth.taps(wl, B * tmax, "prefill", device).view(B, tmax, -1)
+        self.k0, self.v0 = [], []
+        for b in range(B):
+            h = ref.ctx_fuse(self.oc, self.W["w_c"], self.W["g_c"], taps[b, : int(prefix[b])].float().cpu())
+            kv = [ref.ctx_kv(self.oc, self.W["w_qkv"][l], h, 0) for l in range(wl.n_layers)]
+            self.k0.append([k for k, _ in kv])
+            self.v0.append([v for _, v in kv])
+        self.prefix = prefix
+        self.step_taps = synth.taps(wl, B * R, "step", device).float().cpu().view(B, R, -1)
+        self.anchor = synth.anchors(wl)
+        self.target = synth.target_logits(wl, "step", device, torch.float32).cpu().numpy()
+
+    def step(self):
+        ref, wl, W = self.ref, self.wl, self.W
+        out = []
+        for b in range(wl.batch):
+            n0 = int(self.prefix[b])
+            h = ref.ctx_fuse(self.oc, W["w_c"], W["g_c"], self.step_taps[b])
+            ks, vs = [], []
+            for l in range(wl.n_layers):
+                k, v = ref.ctx_kv(self.oc, W["w_qkv"][l], h, n0)
+                ks.append(np.concatenate([self.k0[b][l], k], axis=1))
+                vs.append(np.concatenate([self.v0[b][l], v], axis=1))
+            d = ref.draft_block(self.oc, W, int(self.anchor[b]), ks, vs, n0 + wl.rows)
+            out.append(ref.verify_accept(self.target[b], d["draft"]))
+        return out
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, W, device, steps: int, unit_tokens: int):
+    t0 = time.perf_counter()
+    oc = OracleCycle(wl, W, device)
+    setup_s = time.perf_counter() - t0
+    oc.step()                               # untimed first pass
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oc.step()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": unit_tokens / dt, "unit": "drafted tokens/s", "cores": oracle_threads(),
+            "kind": "oracle", "s_per_step": dt,
+            "sample": f"{steps} full drafting cycles of the same workload (fusion + injection of "
+                      f"{wl.rows} rows, {wl.n_layers}-layer draft over the context, verify), "
+                      f"float64 numpy on the host; weight conversion and prefix prefill "
+                      f"({setup_s:.1f} s) excluded"}
+
+
+METRIC = "draft-block step µs & drafted tokens/s (Qwen3-8B-shape drafter), % HBM roofline"
+
+
+def traffic_from_profile(kernel_file: str, profile: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current source, else None."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, "block_diffusion_drafter_gb300", "csrc", kernel_file), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()[:16]
+        rec = {}
+        for line in open(os.path.join(ROOT, "profiles", profile)):
+            if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes_per_launch")):
+                k, v = line.strip().lstrip("-* ").split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+        if rec.get("source_sha256") == sha:
+            return float(rec["traffic_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def run_gpu(args):
+    rank, local, world = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    import block_diffusion_drafter_gb300 as dfl
+    dfl.load()
+    wl = synth.WORKLOADS[args.workload]
+    hbm, tf_burst, tf_sus, peak_src = measured_peaks()
+    cyc = DraftCycle(dfl, wl, dev)
+    tokens = wl.batch * wl.gamma
+    for _ in range(max(args.warmup, 3)):
+        cyc.step()
+    torch.cuda.synchronize()
+    graph, graph_note = None, "cuda graph replay of the whole step"
+    if not args.no_graph:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                cyc.step()
+            torch.cuda.current_stream().wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cyc.step()
+            graph = g
+        except Exception as e:  # capture unsupported: fall back to eager launches
+            graph, graph_note = None, f"eager launches (graph capture failed: {type(e).__name__})"
+    else:
+        graph_note = "eager launches"
+    fn = graph.replay if graph is not None else cyc.step
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        fn()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    t_end = time.time() + 0.6                  # bring clocks to steady state under load
+    while time.time() < t_end:
+        fn()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = time_steps(fn, args.steps, stream)
+    clocks = sampler.stop()
+    st = int(cyc.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {dfl.status_string(st)}")
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * tokens * args.steps / (ms * 1e-3)
+
+    # end to end through host buffers: inputs H2D from pinned memory, results D2H
+    h_taps = cyc.step_taps.cpu().pin_memory()
+    h_target = cyc.target.cpu().pin_memory()
+    h_anchor = cyc.anchor.cpu().pin_memory()
+    o_draft = torch.empty_like(cyc.draft, device="cpu").pin_memory()
+    o_tau = torch.empty_like(cyc.tau, device="cpu").pin_memory()
+    o_comm = torch.empty_like(cyc.committed, device="cpu").pin_memory()
+
+    def e2e_step():
+        cyc.step_taps.copy_(h_taps, non_blocking=True)
+        cyc.target.copy_(h_target, non_blocking=True)
+        cyc.anchor.copy_(h_anchor, non_blocking=True)
+        fn()
+        o_draft.copy_(cyc.draft, non_blocking=True)
+        o_tau.copy_(cyc.tau, non_blocking=True)
+        o_comm.copy_(cyc.committed, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_e2e = time_steps(e2e_step, args.steps, stream)
+    h2d = h_taps.numel() * h_taps.element_size() + h_target.numel() * 4 + h_anchor.numel() * 4
+    d2h = (o_draft.numel() + o_tau.numel() + o_comm.numel()) * 4
+
+    launches = cyc.launches_per_step()
+    kern = kernel_roofline(cyc, hbm)
+    g = kern.get("gemm_tc", {})
+    traffic = traffic_from_profile("gemm.cu", f"gemm_tc_{args.workload}.md")
+    roof = {"kernel": "gemm_tc (every projection launch of a step: QKV, O, gate|up, down, LM head, "
+                      "fusion, injection)",
+            "bound": "hbm", "achieved": round(g.get("achieved_gbs", 0.0), 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(g.get("frac_of_hbm", 0.0), 4),
+            "traffic": traffic, "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    step_bytes = sum(v["bytes_per_launch"] * v["launches_per_step"] for v in kern.values())
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline(wl, cyc.W, dev, args.cpu_steps, tokens)
+        except MemoryError:
+            cpu = {"value": None, "kind": "oracle", "sample": "host out of memory"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "drafted tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+            "us_per_step": round(1000 * ms / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) taps and target logits)",
+            "config": {"workload": wl.name, "layers": wl.n_layers, "batch_per_gpu": wl.batch,
+                       "context": wl.ctx, "gamma": wl.gamma, "inject_rows_per_step": wl.rows,
+                       "vocab": wl.vocab, "launch": graph_note,
+                       "l2": "inputs larger than L2 (weights streamed per step: "
+                             f"{step_bytes / 1e9:.2f} GB)", "parallelism": f"replicas x{world}"},
+            "clocks": clocks,
+            "e2e": {"value": round(world * tokens * args.steps / (ms_e2e * 1e-3), 1),
+                    "unit": "drafted tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "roofline": roof,
+            "step_roofline": {"algorithmic_bytes": step_bytes, "achieved_gbs": round(step_bytes / (ms / args.steps * 1e-3) / 1e9, 1),
+                              "frac": round(step_bytes / (ms / args.steps * 1e-3) / 1e9 / hbm, 4)},
+            "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        for k, v in kern.items()},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = synth.weights(wl, dev)
+    oc = OracleCycle(wl, W, dev)
+    del W
+    tokens = wl.batch * wl.gamma
+    t0 = time.perf_counter()
+    for _ in range(max(1, args.warmup)):
+        oc.step()
+        if time.perf_counter() - t0 > 60:
+            break
+    t1 = time.perf_counter()
+    oc.step()
+    one = time.perf_counter() - t1
+    steps = max(1, min(args.steps, int(120.0 / max(one, 1e-3))))
+    t1 = time.perf_counter()
+    for _ in range(steps):
+        oc.step()
+    dt = (time.perf_counter() - t1) / steps
+    value = tokens / dt
+    sample = (f"{steps} of {args.steps} requested full drafting cycles timed (each "
+              f"{dt:.2f} s), float64 numpy oracle on the host")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "drafted tokens/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name},
+        "cpu_baseline": {"value": round(value, 3), "unit": "drafted tokens/s", "kind": "oracle",
+                         "cores": oracle_threads(), "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "drafted tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,136 @@
+// Host-side interfaces shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dflash.h"
+
+namespace dfl {
+
+constexpr int kBM = 128;        // MMA M: rows of the A operand per tile
+constexpr int kMaxBN = 512;     // B-operand rows per tile (two MMAs of <= 256)
+constexpr int kGemmThreads = 192;
+constexpr int kMaxGemmCounters = 8192;
+
+// Epilogue operations of the projection GEMM.
+enum EpiOp : int {
+  EPI_STORE = 0,    // out[tok, feat] = acc                      (out dtype: out_bf16)
+  EPI_ADD_F32 = 1,  // out[tok, feat] += acc                     (fp32 residual stream)
+  EPI_QKV = 2,      // block Q/K/V: RoPE(q) -> q_out; RoPE(k), v -> KV cache scratch rows
+  EPI_KV = 3,       // injected context K/V: RoPE(k), v -> KV cache at ctx_len + t
+  EPI_SWIGLU = 4,   // A tile = 64 gate rows + 64 up rows: out = silu(gate) * up
+  EPI_ARGMAX = 5,   // per token: packed (value, index) max -> keys (+ optional fp32 logits)
+  EPI_FUSE = 6      // context fusion: u -> out (cfg dtype) and per-row sums of squares
+};
+
+struct Epi {
+  int op;
+  void* out;          // EPI_STORE / EPI_ADD_F32 / EPI_SWIGLU / EPI_FUSE / EPI_QKV (q)
+  int ld;             // leading dimension of out (elements)
+  int out_bf16;       // 1: out (and caches) are bf16, 0: fp32
+  int n_tok;          // valid token rows
+  int n_feat;         // valid features
+  // attention-layout fields (EPI_QKV / EPI_KV)
+  void* k_cache;
+  void* v_cache;
+  const int* ctx_len;
+  const int* n_new;   // EPI_KV: rows per sequence; NULL for EPI_QKV
+  int rows_per_seq;   // R for EPI_QKV, Tmax for EPI_KV
+  int layer;          // EPI_QKV: layer; EPI_KV: layer of feature tile 0 (see feat_per_layer)
+  int feat_per_layer; // EPI_KV: 2*Hkv*Dh features per layer (layer = feat / feat_per_layer)
+  int max_batch, n_q_heads, n_kv_heads, head_dim, ncap, reserve;
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_positions;
+  // EPI_ARGMAX
+  unsigned long long* keys;
+  // EPI_FUSE
+  float* row_ss;      // [n_tok, n_ss] partial sums of squares
+  int n_ss;
+};
+
+struct GemmArgs {
+  int m_rows;         // valid rows of the A operand
+  int n_rows;         // valid rows of the B operand
+  int k;              // reduction length in elements
+  int bn;             // B rows per tile (multiple of 16 per MMA)
+  int n_sub;          // MMAs per k-step (bn / n_sub rows each)
+  int kt_per_split;   // k-tiles per split
+  int splits;
+  int m_tiles, n_tiles;
+  // TMA coordinates: row = row0 + (tile % tiles_per_z) * tile_rows, z = z0 + tile / tiles_per_z
+  int a_row0, a_z0, a_tiles_per_z;
+  int b_row0, b_z0, b_tiles_per_z;
+  int a_gateup;       // > 0: A tile = 64 rows at a_row0 + 64*m and 64 rows at a_row0 + a_gateup + 64*m
+  int swap;           // 1: A rows are output features and B rows tokens; 0: the reverse
+  int a_weights;      // 1: A is a weight (independent of earlier kernels): prefetch before PDL wait
+  int tf32;           // 1: fp32 operands through kind::tf32
+  float* partial;     // split-K partial tiles
+  int* counters;      // split-K arrival counters (zero between launches)
+  int* dev_status;
+  Epi epi;
+};
+
+struct GemmPlan {
+  int bn, n_sub, splits, kt_per_split, m_tiles, n_tiles, stages;
+  size_t smem_bytes;
+  size_t partial_bytes;
+};
+
+// Chooses tile shape, split count and pipeline depth for m_tiles A tiles
+// against n_rows B rows over k (elements of elem_bytes each).
+GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
+                   int bn_cap = kMaxBN);
+
+// Builds a 3-D tensor map over a [z][rows][k] row-major operand with a box of
+// (64 or 32 elements of k) x box_rows x 1 and 128-byte swizzle.
+bool make_operand_map(CUtensorMap* map, const void* base, int elem_bytes, uint64_t k,
+                      uint64_t rows, uint64_t zdim, uint32_t box_rows);
+
+cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const GemmArgs& args,
+                        const GemmPlan& plan, cudaStream_t stream, bool pdl);
+
+// Attention over [injected context ; block] for one layer.
+struct AttnArgs {
+  const void* q;          // [B*R, Hq*Dh]
+  const void* k_cache;    // layer slice [max_batch, Hkv, Ncap, Dh]
+  const void* v_cache;
+  const int* ctx_len;     // [B]
+  void* out;              // [B*R, Hq*Dh]
+  float* part;            // split partials
+  int* counters;          // [B*Hkv], zero between launches
+  int* dev_status;
+  int B, R, n_q_heads, n_kv_heads, head_dim, ncap, max_batch;
+  int splits, chunk;      // keys per split (multiple of 64); last split takes the rest
+  int bf16;
+};
+void plan_attention(int B, int R, int Hkv, int max_ctx, int ncap, int* splits, int* chunk);
+size_t attention_partial_bytes(int R, int Hq, int Hkv, int Dh);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
+
+// Small row kernels.
+cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
+                         int bf16, float* h, unsigned long long* keys, int n_keys, int* dev_status,
+                         cudaStream_t s, bool pdl);
+// out row r = RMSNorm(x row src(r)); src(r) = r when mask_rows == 0, else
+// (r / gamma) * R + 1 + r % gamma (the mask rows of each block).
+cudaError_t launch_rmsnorm(const float* x, const void* gain, void* out, int rows, int D, float eps,
+                           int bf16, int mask_rows, int gamma, int R, cudaStream_t s, bool pdl);
+cudaError_t launch_fuse_norm(void* h, const float* row_ss, int n_ss, const void* gain, int T,
+                             int D, float eps, int bf16, cudaStream_t s, bool pdl);
+cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int32_t* draft,
+                                   cudaStream_t s, bool pdl);
+cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
+                              int reserve, int* dev_status, cudaStream_t s, bool pdl);
+cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, int B, int gamma,
+                          int V, int32_t* tau, int32_t* committed, int32_t* next_anchor,
+                          unsigned long long* keys, int* counters, cudaStream_t s, bool pdl);
+cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t s, bool pdl);
+
+int num_sms_of_current_device();
+int verify_chunks(int B, int R, int V);
+
+}  // namespace dfl

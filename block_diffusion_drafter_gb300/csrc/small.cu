@@ -1,0 +1,279 @@
+// Row kernels of the drafting step: block embedding, RMSNorm, the context
+// fusion's normalisation pass, argmax decoding, KV-length advance and the
+// greedy verify-accept. All reductions use a fixed order (deterministic).
+#include "common.cuh"
+#include "internal.h"
+
+namespace dfl {
+namespace {
+
+template <typename Kern, typename... Args>
+cudaError_t launch_ex(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+// Block-wide fp32 sum with a fixed reduction tree (256 threads).
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x < 32) {
+    t = lane < 8 ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) red[8] = t;
+  }
+  __syncthreads();
+  return red[8];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* anchor, int mask_id,
+                                                    int R, int D, int V, float* h,
+                                                    unsigned long long* keys, int n_keys,
+                                                    int* dev_status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int r = blockIdx.x, b = r / R, i = r % R;
+  int id = i == 0 ? anchor[b] : mask_id;
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) report(dev_status, DFLASH_ERR_INVALID_ARG);
+    id = 0;
+  }
+  const T* src = embed + static_cast<size_t>(id) * D;
+  float* dst = h + static_cast<size_t>(r) * D;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) dst[d] = to_f32(src[d]);
+  if (blockIdx.x == 0)
+    for (int k = threadIdx.x; k < n_keys; k += blockDim.x) keys[k] = 0ull;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const T* gain, T* out, int D,
+                                                      float eps, int mask_rows, int gamma, int R) {
+  __shared__ float red[9];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int r = blockIdx.x;
+  const int src = mask_rows ? (r / gamma) * R + 1 + r % gamma : r;
+  const float* xr = x + static_cast<size_t>(src) * D;
+  float ss = 0.f;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) ss += xr[d] * xr[d];
+  ss = block_sum256(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
+  T* o = out + static_cast<size_t>(r) * D;
+  for (int d = threadIdx.x; d < D; d += blockDim.x)
+    o[d] = from_f32<T>(to_f32(gain[d]) * xr[d] * inv);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) fuse_norm_kernel(T* h, const float* row_ss, int n_ss,
+                                                        const T* gain, int D, float eps) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int r = blockIdx.x;
+  float ss = 0.f;
+  for (int s = 0; s < n_ss; ++s) ss += row_ss[static_cast<size_t>(r) * n_ss + s];
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
+  T* row = h + static_cast<size_t>(r) * D;
+  for (int d = threadIdx.x; d < D; d += blockDim.x)
+    row[d] = from_f32<T>(to_f32(gain[d]) * to_f32(row[d]) * inv);
+}
+
+__global__ void argmax_finalize_kernel(unsigned long long* keys, int n, int32_t* draft) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) draft[i] = static_cast<int32_t>(argmax_key_index(keys[i]));
+}
+
+__global__ void kv_advance_kernel(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
+                                  int reserve, int* dev_status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int nn = n_new[b];
+  if (nn < 0 || nn > Tmax) { report(dev_status, DFLASH_ERR_INVALID_ARG); return; }
+  if (ctx_len[b] + nn > ncap - reserve) { report(dev_status, DFLASH_ERR_CAPACITY); return; }
+  ctx_len[b] += nn;
+}
+
+__global__ void copy_f32_kernel(float* dst, const float* src, size_t n) {
+  pdl_launch_dependents();
+  pdl_wait();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
+// Greedy verification. Grid (chunks, R, B): each CTA takes the argmax of one
+// V-slice of target row (b, j) and folds it into keys[b*R + j] with a 64-bit
+// integer max (ties -> lowest index); the last CTA of sequence b scans the
+// R argmaxes against the draft and writes tau / committed / next anchor.
+template <typename T>
+__global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int32_t* draft, int gamma,
+                                                     int V, int chunk, int32_t* tau,
+                                                     int32_t* committed, int32_t* next_anchor,
+                                                     unsigned long long* keys, int* counters) {
+  __shared__ unsigned long long red[8];
+  __shared__ int is_last;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int R = gamma + 1;
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
+  const T* row = logits + (static_cast<size_t>(b) * R + j) * V;
+  unsigned long long best = 0ull;
+  constexpr int kVec = 16 / sizeof(T);
+  if ((V % kVec) == 0 && (chunk % kVec) == 0) {
+    for (int v = v0 + threadIdx.x * kVec; v < v1; v += blockDim.x * kVec) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + v));
+      const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int q = 0; q < kVec; ++q) {
+        const unsigned long long k = argmax_key(to_f32(e[q]), static_cast<uint32_t>(v + q));
+        best = k > best ? k : best;
+      }
+    }
+  } else {
+    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+      const unsigned long long k = argmax_key(to_f32(row[v]), static_cast<uint32_t>(v));
+      best = k > best ? k : best;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+    best = t > best ? t : best;
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long m = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = red[w] > m ? red[w] : m;
+    atomicMax(&keys[b * R + j], m);
+    __threadfence();
+    const int prev = atomicAdd(&counters[b], 1);
+    is_last = prev == gridDim.x * R - 1;
+  }
+  __syncthreads();
+  if (!is_last || threadIdx.x != 0) return;
+  __threadfence();
+  int a = 0;
+  int32_t t_a = 0;
+  for (int jj = 0; jj <= gamma; ++jj) {
+    const int32_t tj = static_cast<int32_t>(argmax_key_index(__ldcg(&keys[b * R + jj])));
+    if (jj == a) {
+      if (jj < gamma && draft[b * gamma + jj] == tj) {
+        committed[b * R + jj] = tj;
+        ++a;
+      } else {
+        t_a = tj;
+      }
+    }
+  }
+  committed[b * R + a] = t_a;
+  for (int jj = a + 1; jj <= gamma; ++jj) committed[b * R + jj] = -1;
+  tau[b] = a + 1;
+  next_anchor[b] = t_a;
+  for (int jj = 0; jj <= gamma; ++jj) keys[b * R + jj] = 0ull;
+  counters[b] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
+                         int bf16, float* h, unsigned long long* keys, int n_keys, int* dev_status,
+                         cudaStream_t s, bool pdl) {
+  if (bf16)
+    return launch_ex(embed_kernel<__nv_bfloat16>, dim3(B * R), dim3(256), 0, s, pdl,
+                     reinterpret_cast<const __nv_bfloat16*>(embed), anchor, mask_id, R, D, V, h, keys,
+                     n_keys, dev_status);
+  return launch_ex(embed_kernel<float>, dim3(B * R), dim3(256), 0, s, pdl,
+                   reinterpret_cast<const float*>(embed), anchor, mask_id, R, D, V, h, keys, n_keys,
+                   dev_status);
+}
+
+cudaError_t launch_rmsnorm(const float* x, const void* gain, void* out, int rows, int D, float eps,
+                           int bf16, int mask_rows, int gamma, int R, cudaStream_t s, bool pdl) {
+  if (bf16)
+    return launch_ex(rmsnorm_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, pdl, x,
+                     reinterpret_cast<const __nv_bfloat16*>(gain),
+                     reinterpret_cast<__nv_bfloat16*>(out), D, eps, mask_rows, gamma, R);
+  return launch_ex(rmsnorm_kernel<float>, dim3(rows), dim3(256), 0, s, pdl, x,
+                   reinterpret_cast<const float*>(gain), reinterpret_cast<float*>(out), D, eps,
+                   mask_rows, gamma, R);
+}
+
+cudaError_t launch_fuse_norm(void* h, const float* row_ss, int n_ss, const void* gain, int T, int D,
+                             float eps, int bf16, cudaStream_t s, bool pdl) {
+  if (bf16)
+    return launch_ex(fuse_norm_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, s, pdl,
+                     reinterpret_cast<__nv_bfloat16*>(h), row_ss, n_ss,
+                     reinterpret_cast<const __nv_bfloat16*>(gain), D, eps);
+  return launch_ex(fuse_norm_kernel<float>, dim3(T), dim3(256), 0, s, pdl, reinterpret_cast<float*>(h),
+                   row_ss, n_ss, reinterpret_cast<const float*>(gain), D, eps);
+}
+
+cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int32_t* draft, cudaStream_t s,
+                                   bool pdl) {
+  return launch_ex(argmax_finalize_kernel, dim3((n + 127) / 128), dim3(128), 0, s, pdl, keys, n, draft);
+}
+
+cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
+                              int reserve, int* dev_status, cudaStream_t s, bool pdl) {
+  return launch_ex(kv_advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s, pdl, ctx_len, n_new, B,
+                   Tmax, ncap, reserve, dev_status);
+}
+
+cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t s, bool pdl) {
+  return launch_ex(copy_f32_kernel, dim3(304), dim3(256), 0, s, pdl, dst, src, n);
+}
+
+int verify_chunks(int B, int R, int V) {
+  int by_size = (V + 4095) / 4096;
+  int by_grid = (2 * 152 + B * R - 1) / (B * R);
+  int c = by_size < by_grid ? by_size : by_grid;
+  return c < 1 ? 1 : c;
+}
+
+cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, int B, int gamma, int V,
+                          int32_t* tau, int32_t* committed, int32_t* next_anchor,
+                          unsigned long long* keys, int* counters, cudaStream_t s, bool pdl) {
+  const int R = gamma + 1;
+  const int chunks = verify_chunks(B, R, V);
+  int chunk = (V + chunks - 1) / chunks;
+  chunk = (chunk + 7) / 8 * 8;
+  const int n_chunks = (V + chunk - 1) / chunk;
+  if (bf16)
+    return launch_ex(verify_kernel<__nv_bfloat16>, dim3(n_chunks, R, B), dim3(256), 0, s, pdl,
+                     reinterpret_cast<const __nv_bfloat16*>(logits), draft, gamma, V, chunk, tau,
+                     committed, next_anchor, keys, counters);
+  return launch_ex(verify_kernel<float>, dim3(n_chunks, R, B), dim3(256), 0, s, pdl,
+                   reinterpret_cast<const float*>(logits), draft, gamma, V, chunk, tau, committed,
+                   next_anchor, keys, counters);
+}
+
+int num_sms_of_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+}  // namespace dfl

@@ -239,6 +239,14 @@ dflash_status dflash_verify_accept(const dflash_config* cfg,
 dflash_status dflash_rope_tables(const dflash_config* cfg, int n_pos,
                                  float* host_cos, float* host_sin);
 
+/* Plain projection y = x W^T, the building block of every projection above
+ * (W_c of [P1] "KV Injection 메커니즘", W^Q/K/V/O and the FFN of the drafter
+ * layers). x: [M, K], w: [N, K] of `dtype`; y: [M, N] fp32. K must be a
+ * multiple of 64 (bf16) or 32 (fp32). Runs on the same tcgen05 kernel as the
+ * drafting step; `ws` needs dflash_workspace_bytes of any valid config. */
+dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, float* y, int M,
+                            int N, int K, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

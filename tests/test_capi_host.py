@@ -1,0 +1,117 @@
+"""Host-side checks of the C-ABI library: it loads, exports every function
+that include/dflash.h declares, and its pure-host calls (config checks,
+sizing, RoPE tables, argument validation) behave without a GPU."""
+import ctypes
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "memory_table.txt")
+
+
+def read_golden():
+    out = {}
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, val, tol = line.split()[:3]
+        out[key] = (float(val), float(tol))
+    return out
+
+
+def test_library_exports_every_header_function(lib):
+    names = lib.header_functions()
+    assert "dflash_draft_block" in names and "dflash_verify_accept" in names
+    so = ctypes.CDLL(lib.lib_path())
+    missing = [n for n in names if not hasattr(so, n)]
+    assert not missing, missing
+    assert lib.load().dflash_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(0, -10, -1):
+        assert lib.status_string(s) != "unknown status"
+    assert lib.status_string(-99) == "unknown status"
+
+
+def test_workload_configs_are_accepted(lib):
+    for wl in synth.WORKLOADS.values():
+        cfg = lib.config_from_workload(wl)
+        assert lib.dflash_check_config(cfg) == lib.OK, wl.name
+        assert lib.dflash_workspace_bytes(cfg, 4096) > 0
+
+
+def test_bad_configs_are_rejected(lib):
+    wl = synth.WORKLOADS["qwen3_8b_L5_N2048_B1"]
+    good = lib.config_from_workload(wl)
+    for field, value, want in [("gamma", 0, lib.ERR_INVALID_ARG), ("gamma", 17, lib.ERR_INVALID_ARG),
+                               ("head_dim", 96, lib.ERR_SHAPE), ("n_kv_heads", 5, lib.ERR_SHAPE),
+                               ("d_model", 4000, lib.ERR_SHAPE), ("dtype", 7, lib.ERR_DTYPE),
+                               ("mask_token_id", wl.vocab, lib.ERR_INVALID_ARG),
+                               ("ctx_capacity", 10, lib.ERR_INVALID_ARG)]:
+        cfg = lib.make_config(*[getattr(good, f) for f, _ in lib.Config._fields_])
+        setattr(cfg, field, value)
+        assert lib.dflash_check_config(cfg) == want, field
+
+
+def test_memory_table_of_the_pages(lib):
+    """W_c and the fusion's activations for the page's D = 2048 bf16 example."""
+    g = read_golden()
+    cfg = lib.make_config(5, 2048, 5, 2048, 16, 4, 128, 6144, 32000, 16, 31999, 1, 4096)
+    wc = lib.dflash_param_bytes(cfg, 0)
+    assert wc == 5 * 2048 * 2048 * 2
+    v, tol = g["w_c_param_bytes"]
+    assert abs(wc - v) / v <= tol
+    seq = 2048
+    fin = seq * cfg.n_taps * cfg.d_target * 2
+    fout = seq * cfg.d_model * 2
+    for key, got in [("fuse_input_activation_bytes", fin), ("fuse_output_activation_bytes", fout)]:
+        v, tol = g[key]
+        assert abs(got - v) / v <= tol, key
+    # decode time: the same projection over one block of 16 rows (in + out)
+    blk = 16 * cfg.n_taps * cfg.d_target * 2 + 16 * cfg.d_model * 2
+    assert blk < g["decode_block_activation_max"][0]
+
+
+def test_param_bytes_of_qwen3_8b_shape(lib):
+    wl = synth.WORKLOADS["qwen3_8b_L5_N2048_B1"]
+    cfg = lib.config_from_workload(wl)
+    per_layer = ((32 + 16) * 128 * 4096 + 4096 * 4096 + 2 * 12288 * 4096 + 4096 * 12288 + 2 * 4096) * 2
+    assert lib.dflash_param_bytes(cfg, 3) == 5 * per_layer
+    assert lib.dflash_param_bytes(cfg, 2) == 151936 * 4096 * 2
+    assert lib.dflash_kv_cache_bytes(cfg) == 5 * 1 * 8 * wl.capacity() * 128 * 2
+
+
+def test_rope_tables_match_closed_form(lib):
+    cfg = lib.config_from_workload(synth.WORKLOADS["tiny_f32_L1_N128"])
+    c, s = lib.dflash_rope_tables(cfg, 300)
+    half = cfg.head_dim // 2
+    p = np.arange(300)[:, None]
+    j = np.arange(half)[None, :]
+    ang = p * cfg.rope_theta ** (-2.0 * j / cfg.head_dim)
+    np.testing.assert_allclose(c.numpy(), np.cos(ang), atol=2e-7)
+    np.testing.assert_allclose(s.numpy(), np.sin(ang), atol=2e-7)
+
+
+def test_null_arguments_rejected_before_any_launch(lib):
+    L = lib.load()
+    cfg = lib.config_from_workload(synth.WORKLOADS["tiny_f32_L1_N128"])
+    w = lib.WeightsStruct()
+    assert L.dflash_draft_block(ctypes.byref(cfg), ctypes.byref(w), None, None, 1, 0, None, None,
+                                None, None, None, None, None, 0, None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_verify_accept(ctypes.byref(cfg), None, 0, None, 1, None, None, None, None, 0,
+                                  None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_kv_inject(ctypes.byref(cfg), ctypes.byref(w), None, None, 1, 4, None, None,
+                              None, None, None, 0, None) == lib.ERR_INVALID_ARG
+    # T == 0 and B == 0 are no-ops
+    assert L.dflash_ctx_fuse(ctypes.byref(cfg), ctypes.byref(w), None, 0, None, None, 0, None) == lib.OK
+    assert L.dflash_kv_inject(ctypes.byref(cfg), ctypes.byref(w), None, None, 0, 4, None, None,
+                              None, None, None, 0, None) == lib.OK
+    # batch beyond max_batch
+    assert L.dflash_verify_accept(ctypes.byref(cfg), 1, 0, 1, cfg.max_batch + 1, 1, 1, 1, 1, 1,
+                                  None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_linear(5, None, None, None, 1, 1, 64, None, 0, None) == lib.ERR_DTYPE
