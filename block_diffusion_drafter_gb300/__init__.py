@@ -254,6 +254,9 @@ class TraceRecorder:
     def __init__(self, capacity: int = 512):
         self.capacity = capacity
         self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.ev:      # torch creates the CUDA event on first record
+            e.record()
+        torch.cuda.synchronize()
         self._events = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.ev])
         self._kinds = (ctypes.c_int * capacity)()
         self._bytes = (ctypes.c_double * capacity)()

@@ -86,6 +86,10 @@ WORKLOADS = {
     "qwen3_8b_L5_ragged_B16": Workload(
         "qwen3_8b_L5_ragged_B16", n_layers=5, batch=16, ctx=8192, ctx_min=512,
         seed=1004, **_QWEN3_8B),
+    # one-layer version of the same shapes: small enough (~3 GB on the device)
+    # for kernel-level profiler captures
+    "qwen3_8b_L1_N2048_B1": Workload(
+        "qwen3_8b_L1_N2048_B1", n_layers=1, batch=1, ctx=2048, seed=1006, **_QWEN3_8B),
     # full draft-verify loop: 8 layers, batch 4, context 4096, 256 cycles
     "qwen3_8b_L8_loop_B4": Workload(
         "qwen3_8b_L8_loop_B4", n_layers=8, batch=4, ctx=4096, cycles=256,

@@ -36,6 +36,7 @@ def assert_act_close(gpu, want, what, tol=ACT_TOL):
     rms = float(np.sqrt(np.mean(w * w)))
     err = float(np.max(np.abs(g - w))) if w.size else 0.0
     assert err <= tol * rms, f"{what}: max abs err {err:.3e} > {tol} * rms {rms:.3e}"
+    report(what, "max_abs_err/rms", err / max(rms, 1e-30), tol)
     return err / max(rms, 1e-30)
 
 
@@ -44,6 +45,7 @@ def assert_logits_close(gpu, want, what="logits", tol=LOGIT_TOL):
     w = np.asarray(want, dtype=np.float64)
     rel = float(np.sqrt(np.mean((g - w) ** 2)) / np.sqrt(np.mean(w * w)))
     assert rel <= tol, f"{what}: relative rms err {rel:.3e} > {tol}"
+    report(what, "rms_err/rms", rel, tol)
     return rel
 
 
@@ -57,7 +59,19 @@ def assert_drafts_match(gpu_draft, oracle_logits, what="draft"):
     bad = (d != want) & (margin >= MARGIN)
     assert not bad.any(), f"{what}: {int(bad.sum())} tokens differ outside near-ties " \
                           f"(rows {np.nonzero(bad)[0][:8].tolist()})"
-    return int((d != want).sum())
+    n_diff = int((d != want).sum())
+    report(what, "tokens_differing_at_near_ties", n_diff, 0)
+    return n_diff
+
+
+def report(what, measure, value, tol):
+    """Appends one parity measurement to $DFLASH_PARITY_LOG (if set)."""
+    import json
+    import os
+    path = os.environ.get("DFLASH_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, "measure": measure, "value": value, "tol": tol}) + "\n")
 
 
 class GpuDrafter:
