@@ -21,6 +21,7 @@ namespace {
 constexpr int kKeyTile = 64;
 constexpr int kStagesKV = 3;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxAttnCluster = 16;  // split-KV CTAs of one (sequence, KV head): one cluster
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
@@ -259,52 +260,71 @@ __global__ void __launch_bounds__(256) attn_bf16_kernel(const AttnArgs p) {
     return;
   }
 
-  const int cta = (b * p.n_kv_heads + kvh) * p.splits + s;
-  float* po = p.part + static_cast<size_t>(cta) * qr_pad * DH;
-  float2* pml = reinterpret_cast<float2*>(p.part + static_cast<size_t>(p.B) * p.n_kv_heads * p.splits * qr_pad * DH) +
-                static_cast<size_t>(cta) * qr_pad;
+  // Split-KV merge inside the cluster of this (sequence, KV head): every CTA
+  // parks its unnormalised O rows and (m, l) in its own shared memory; after
+  // the barrier, CTA r merges a slice of the rows by reading all splits
+  // through distributed shared memory (ascending split order), weighting each
+  // split by 2^(m_s - M) / L. The second barrier keeps the partials alive
+  // until every peer has read them.
+  __syncthreads();  // the K/V ring is drained: reuse it for the partials
+  float* po_s = reinterpret_cast<float*>(k_s);                        // [qr_pad][DH]
+  float2* ml_s = reinterpret_cast<float2*>(po_s + qr_pad * DH);       // [qr_pad]
+  float* w_loc = reinterpret_cast<float*>(ml_s + qr_pad);             // [rows of this CTA][splits]
 #pragma unroll
   for (int i = 0; i < DH / 8; ++i) {
     const int d = i * 8 + 2 * t4;
-    __stcg(reinterpret_cast<float2*>(&po[qr0 * DH + d]), make_float2(o[i][0], o[i][1]));
-    __stcg(reinterpret_cast<float2*>(&po[qr1 * DH + d]), make_float2(o[i][2], o[i][3]));
+    *reinterpret_cast<float2*>(&po_s[qr0 * DH + d]) = make_float2(o[i][0], o[i][1]);
+    *reinterpret_cast<float2*>(&po_s[qr1 * DH + d]) = make_float2(o[i][2], o[i][3]);
   }
   if (t4 == 0) {
-    __stcg(&pml[qr0], make_float2(m0, l0));
-    __stcg(&pml[qr1], make_float2(m1, l1));
+    ml_s[qr0] = make_float2(m0, l0);
+    ml_s[qr1] = make_float2(m1, l1);
   }
-  __threadfence();
-  __syncthreads();
-  __shared__ int is_last;
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(&p.counters[b * p.n_kv_heads + kvh], 1);
-    is_last = prev == p.splits - 1;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  const int cta0 = (b * p.n_kv_heads + kvh) * p.splits;
-  const float* po0 = p.part + static_cast<size_t>(cta0) * qr_pad * DH;
-  const float2* pml0 = reinterpret_cast<const float2*>(p.part + static_cast<size_t>(p.B) * p.n_kv_heads * p.splits * qr_pad * DH) +
-                       static_cast<size_t>(cta0) * qr_pad;
-  for (int idx = threadIdx.x; idx < n_q * DH; idx += blockDim.x) {
-    const int qr = idx / DH, d = idx % DH;
+  cluster_sync();
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int per = (n_q + p.splits - 1) / p.splits;
+  const int r0 = rank * per, r1 = min(n_q, r0 + per);
+  const uint32_t po_u = smem_u32(po_s), ml_u = smem_u32(ml_s);
+  for (int qr = r0 + static_cast<int>(threadIdx.x); qr < r1; qr += blockDim.x) {
     float M = -INFINITY;
     for (int sp = 0; sp < p.splits; ++sp) {
-      const float2 ml = __ldcg(&pml0[sp * qr_pad + qr]);
+      float2 ml;
+      asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                   : "=f"(ml.x), "=f"(ml.y)
+                   : "r"(mapa_shared(ml_u + qr * 8, sp))
+                   : "memory");
+      w_loc[(qr - r0) * p.splits + sp] = ml.y > 0.f ? ml.x : -INFINITY;
+      w_loc[(qr - r0) * p.splits + sp + per * p.splits] = ml.y;
       if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
-    float L = 0.f, acc = 0.f;
+    float L = 0.f;
     for (int sp = 0; sp < p.splits; ++sp) {
-      const float2 ml = __ldcg(&pml0[sp * qr_pad + qr]);
-      if (!(ml.y > 0.f)) continue;
-      const float w = exp2f(ml.x - M);
-      L += ml.y * w;
-      acc += __ldcg(&po0[(static_cast<size_t>(sp) * qr_pad + qr) * DH + d]) * w;
+      const float m = w_loc[(qr - r0) * p.splits + sp];
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      w_loc[(qr - r0) * p.splits + sp] = w;
+      L += w_loc[(qr - r0) * p.splits + sp + per * p.splits] * w;
     }
-    out[out_index(qr, d)] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int sp = 0; sp < p.splits; ++sp) w_loc[(qr - r0) * p.splits + sp] *= inv;
   }
-  if (threadIdx.x == 0) p.counters[b * p.n_kv_heads + kvh] = 0;
+  __syncthreads();
+  constexpr int D4 = DH / 4;
+  const int n_items = (r1 > r0 ? r1 - r0 : 0) * D4;
+  for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
+    const int qr = r0 + it / D4, d = (it % D4) * 4;
+    const uint32_t off = po_u + static_cast<uint32_t>((qr * DH + d) * 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = 0; sp < p.splits; ++sp) {
+      const float w = w_loc[(qr - r0) * p.splits + sp];
+      const float4 v = ld_dsmem_f4(mapa_shared(off, sp));
+      acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
+    }
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(&out[out_index(qr, d)]);
+    dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    dst[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+  cluster_sync();
 }
 
 }  // namespace
@@ -376,28 +396,24 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
 
 }  // namespace
 
-void plan_attention(int B, int R, int Hkv, int max_ctx, int ncap, int* splits, int* chunk) {
+void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
+                    int* chunk) {
   const int n_keys = (max_ctx < ncap ? max_ctx : ncap) + R;
   const int per_seq = B * Hkv > 0 ? B * Hkv : 1;
   int target = (2 * 152 + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
+  if (target > kMaxAttnCluster) target = kMaxAttnCluster;
   int c = (n_keys + target - 1) / target;
   c = (c + kKeyTile - 1) / kKeyTile * kKeyTile;
-  if (c < 256) c = 256;
+  if (c < 128) c = 128;
   int sp = (n_keys + c - 1) / c;
-  if (sp < 1) sp = 1;
-  // the partial buffer holds at most 640 CTAs
-  while (sp > 1 && per_seq * sp > 640) {
+  while (sp > kMaxAttnCluster) {
     c += kKeyTile;
     sp = (n_keys + c - 1) / c;
   }
-  *splits = sp;
+  *splits = sp < 1 ? 1 : sp;
   *chunk = c;
-}
-
-size_t attention_partial_bytes(int R, int Hq, int Hkv, int Dh) {
-  const int G = Hq / Hkv;
-  const int qr_pad = (G * R + 15) / 16 * 16;
-  return static_cast<size_t>(640) * qr_pad * (Dh + 2) * sizeof(float);
+  (void)Hq;
+  (void)Dh;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl) {
@@ -431,9 +447,27 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   bool& done = configured[a.head_dim == 128][dev & 63];
   if (!done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     done = true;
   }
+  if (a.splits > kMaxAttnCluster) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr2[2];
+  int n = 0;
+  if (pdl) {
+    attr2[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr2[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (a.splits > 1) {
+    attr2[n].id = cudaLaunchAttributeClusterDimension;
+    attr2[n].val.clusterDim.x = a.splits;
+    attr2[n].val.clusterDim.y = 1;
+    attr2[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr2 : nullptr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

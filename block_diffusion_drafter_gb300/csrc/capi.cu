@@ -19,19 +19,10 @@ inline int elem_bytes(const dflash_config* c) { return c->dtype == DFLASH_BF16 ?
 inline int rows_per_block(const dflash_config* c) { return c->gamma + 1; }
 
 struct WsLayout {
-  size_t h, xn, q, attn_o, act, z, lm_keys, v_keys, v_count, gemm_counters, attn_counters;
-  size_t gemm_partial, attn_part, row_ss;
+  size_t h, xn, q, attn_o, act, z, lm_keys, v_keys, v_count;
+  size_t row_ss;
   size_t fixed;  // bytes before row_ss
-  size_t partial_bytes, attn_part_bytes;
 };
-
-// Upper bound of the split-K partial buffer: a plan never puts more than
-// (SMs x CTAs per SM) split CTAs on a tile set, each holding bn x 128 floats.
-size_t gemm_partial_bound() {
-  const size_t a = static_cast<size_t>(2 * kNumSmsUpperBound) * 64 * kBM * 4;
-  const size_t b = static_cast<size_t>(kNumSmsUpperBound) * kMaxBN * kBM * 4;
-  return a > b ? a : b;
-}
 
 WsLayout ws_layout(const dflash_config* c) {
   WsLayout L{};
@@ -50,12 +41,6 @@ WsLayout ws_layout(const dflash_config* c) {
   L.lm_keys = take(static_cast<size_t>(c->max_batch) * c->gamma * 8);
   L.v_keys = take(rows * 8);
   L.v_count = take(static_cast<size_t>(c->max_batch) * 4);
-  L.gemm_counters = take(static_cast<size_t>(kMaxGemmCounters) * 4);
-  L.attn_counters = take(static_cast<size_t>(c->max_batch) * c->n_kv_heads * 4);
-  L.partial_bytes = gemm_partial_bound();
-  L.gemm_partial = take(L.partial_bytes);
-  L.attn_part_bytes = attention_partial_bytes(static_cast<int>(R), c->n_q_heads, c->n_kv_heads, c->head_dim);
-  L.attn_part = take(L.attn_part_bytes);
   L.row_ss = off;
   L.fixed = off;
   return L;
@@ -226,17 +211,6 @@ dflash_status dflash_rope_tables(const dflash_config* c, int n_pos, float* host_
 
 namespace {
 
-// Fits a plan's split count to the partial buffer.
-void fit_partial(GemmPlan& p, size_t cap) {
-  while (p.splits > 1 && p.partial_bytes > cap) {
-    const int KT = p.kt_per_split * p.splits;
-    p.kt_per_split = (KT + p.splits - 2) / (p.splits - 1);
-    p.splits = (KT + p.kt_per_split - 1) / p.kt_per_split;
-    p.partial_bytes = static_cast<size_t>(p.m_tiles) * p.n_tiles * p.splits * p.bn * kBM * 4;
-  }
-  if (p.splits <= 1) p.partial_bytes = 0;
-}
-
 void fill_from_plan(GemmArgs& g, const GemmPlan& p, int k) {
   g.k = k;
   g.bn = p.bn;
@@ -263,13 +237,8 @@ struct Ctx {
 // One projection launch: A rows a_rows (weights when swap), B rows b_rows.
 dflash_status run_gemm(Ctx& x, GemmArgs g, const CUtensorMap& amap, const CUtensorMap& bmap,
                        GemmPlan plan, double bytes, double flops) {
-  fit_partial(plan, x.L.partial_bytes);
   fill_from_plan(g, plan, g.k);
   g.tf32 = x.c->dtype == DFLASH_F32;
-  g.partial = at<float>(x.ws, x.L.gemm_partial);
-  g.counters = at<int>(x.ws, x.L.gemm_counters);
-  if (static_cast<long long>(g.m_tiles) * g.n_tiles > kMaxGemmCounters && g.splits > 1)
-    return DFLASH_ERR_SHAPE;
   x.tr.before(DFLASH_K_GEMM, bytes, flops);
   const cudaError_t e = launch_gemm(amap, bmap, g, plan, x.s, x.pdl);
   x.tr.after();
@@ -305,17 +274,14 @@ dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, fl
   if (x == nullptr || w == nullptr || y == nullptr) return DFLASH_ERR_INVALID_ARG;
   const int es = dtype == DFLASH_BF16 ? 2 : 4;
   if (K % (128 / es)) return DFLASH_ERR_SHAPE;
-  const size_t need = align256(static_cast<size_t>(kMaxGemmCounters) * 4) + gemm_partial_bound();
-  if (ws == nullptr || ws_bytes < need) return DFLASH_ERR_WORKSPACE;
+  (void)ws;
+  (void)ws_bytes;
   dflash_status st = check_arch();
   if (st != DFLASH_OK) return st;
   dflash_config cfg{};
   cfg.dtype = dtype;
   Ctx cx{&cfg, WsLayout{}, ws, reinterpret_cast<cudaStream_t>(stream), es, num_sms_of_current_device(),
          use_pdl(), Tracer{nullptr, nullptr}};
-  cx.L.gemm_counters = 0;
-  cx.L.gemm_partial = align256(static_cast<size_t>(kMaxGemmCounters) * 4);
-  cx.L.partial_bytes = gemm_partial_bound();
   GemmArgs g{};
   CUtensorMap amap, bmap;
   GemmPlan plan;
@@ -544,7 +510,8 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
     return DFLASH_ERR_CUDA;
 
   int a_splits = 1, a_chunk = 0;
-  plan_attention(B, R, c->n_kv_heads, max_ctx_hint, c->ctx_capacity, &a_splits, &a_chunk);
+  plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, c->ctx_capacity,
+                 &a_splits, &a_chunk);
 
   for (int l = 0; l < Lyr; ++l) {
     const size_t gain_off = static_cast<size_t>(l) * D * es;
@@ -577,8 +544,6 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
       a.k_cache = static_cast<const uint8_t*>(k_cache) + l * layer_kv;
       a.v_cache = static_cast<const uint8_t*>(v_cache) + l * layer_kv;
       a.ctx_len = ctx_len; a.out = ao;
-      a.part = at<float>(ws, L.attn_part);
-      a.counters = at<int>(ws, L.attn_counters);
       a.dev_status = dev_status;
       a.B = B; a.R = R; a.n_q_heads = c->n_q_heads; a.n_kv_heads = c->n_kv_heads;
       a.head_dim = c->head_dim; a.ncap = c->ctx_capacity; a.max_batch = c->max_batch;

@@ -11,8 +11,9 @@
 //    from HBM exactly once and the token tile rides along as the MMA's N.
 //  - plain (A = tokens, B = weight rows): context fusion / injection over
 //    long prefills, which is tensor-bound.
-// Split-K partial tiles are reduced by the last-arriving CTA of a tile in a
-// fixed split order (deterministic; no float atomics, no inter-CTA waits).
+// Split-K runs as a thread-block cluster per output tile: the partial tiles
+// meet in distributed shared memory and are summed in a fixed split order
+// (deterministic; no float atomics, no global partial buffers).
 #include <stdio.h>
 
 #include "common.cuh"
@@ -25,6 +26,8 @@ namespace dfl {
 namespace {
 
 constexpr int kSLD = 129;  // staging row stride (floats): conflict-free both ways
+// barriers + token table, plus slack to align the tile ring to 1024 bytes
+constexpr size_t kSmemHeaderBytes = 4096;
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
@@ -47,27 +50,75 @@ __device__ __forceinline__ float rope_rot(const Epi& e, int pos, int d, float x,
 
 // Applies the epilogue to one staged chunk: S[b * kSLD + a] holds C for
 // A-row a (0..127) and B-row col0 + b (0 <= b < cols) of tile (m_tile, n_tile).
-// Runs on the 128 epilogue threads (etid 0..127).
-__device__ void apply_epilogue(const GemmArgs& g, const float* S, int col0, int cols, int m_tile,
-                               int n_tile, int etid) {
+// Runs on the 128 epilogue threads (etid 0..127). Every op works in batches
+// of kEpiBatch elements per thread: all global loads of a batch are issued
+// before any of its stores, so the loads overlap instead of serialising
+// behind possibly-aliasing stores.
+constexpr int kEpiBatch = 8;
+
+struct TokInfo {
+  int pos[kBM];   // cache position of the tile's token x, -1 = skip
+  int seq[kBM];   // sequence of token x
+};
+
+__device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, int col0, int cols,
+                               int m_tile, int n_tile, int etid) {
   const Epi& e = g.epi;
   const int total = cols * kBM;
+  const bool tok_cols = g.swap != 0;  // tokens along B rows (columns of S)
+  if (e.op == EPI_QKV || e.op == EPI_KV) {
+    const int nloc = tok_cols ? cols : kBM;
+    for (int x = etid; x < nloc; x += 128) {
+      const int tok = tok_cols ? n_tile * g.bn + col0 + x : m_tile * kBM + x;
+      int pos = -1, seq = 0;
+      if (tok < e.n_tok) {
+        seq = tok / e.rows_per_seq;
+        const int t = tok - seq * e.rows_per_seq;
+        const int base = e.ctx_len[seq];
+        if (e.op == EPI_QKV) {
+          pos = base + t;
+          if (pos >= e.ncap) { report(g.dev_status, DFLASH_ERR_CAPACITY); pos = -1; }
+        } else {
+          const int nn = e.n_new[seq];
+          if (t < nn && base + nn <= e.ncap - e.reserve) pos = base + t;
+        }
+      }
+      ti->pos[x] = pos;
+      ti->seq[x] = seq;
+    }
+    named_bar(1, 128);
+  }
   switch (e.op) {
     case EPI_STORE:
     case EPI_ADD_F32:
     case EPI_FUSE: {
-      for (int idx = etid; idx < total; idx += 128) {
-        int a, b;
-        if (g.swap) { a = idx & 127; b = idx >> 7; } else { b = idx % cols; a = idx / cols; }
-        const int feat = g.swap ? m_tile * kBM + a : n_tile * g.bn + col0 + b;
-        const int tok = g.swap ? n_tile * g.bn + col0 + b : m_tile * kBM + a;
-        if (tok >= e.n_tok || feat >= e.n_feat) continue;
-        const float v = S[b * kSLD + a];
-        const size_t o = static_cast<size_t>(tok) * e.ld + feat;
-        if (e.op == EPI_ADD_F32)
-          reinterpret_cast<float*>(e.out)[o] += v;
-        else
-          store_out(e.out, e.out_bf16, o, v);
+      for (int base = etid; base < total; base += 128 * kEpiBatch) {
+        float v[kEpiBatch], r[kEpiBatch];
+        size_t o[kEpiBatch];
+        bool ok[kEpiBatch];
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int idx = base + u * 128;
+          int a, b;
+          if (g.swap) { a = idx & 127; b = idx >> 7; } else { b = idx % cols; a = idx / cols; }
+          const int feat = g.swap ? m_tile * kBM + a : n_tile * g.bn + col0 + b;
+          const int tok = g.swap ? n_tile * g.bn + col0 + b : m_tile * kBM + a;
+          ok[u] = idx < total && tok < e.n_tok && feat < e.n_feat;
+          v[u] = ok[u] ? S[b * kSLD + a] : 0.f;
+          o[u] = static_cast<size_t>(tok) * e.ld + feat;
+        }
+        if (e.op == EPI_ADD_F32) {
+#pragma unroll
+          for (int u = 0; u < kEpiBatch; ++u)
+            r[u] = ok[u] ? reinterpret_cast<const float*>(e.out)[o[u]] : 0.f;
+#pragma unroll
+          for (int u = 0; u < kEpiBatch; ++u)
+            if (ok[u]) reinterpret_cast<float*>(e.out)[o[u]] = r[u] + v[u];
+        } else {
+#pragma unroll
+          for (int u = 0; u < kEpiBatch; ++u)
+            if (ok[u]) store_out(e.out, e.out_bf16, o[u], v[u]);
+        }
       }
       if (e.op == EPI_FUSE) {
         // Per token: sum of squares over this chunk's 128 features, summed
@@ -104,61 +155,81 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, int col0, int 
       }
       break;
     }
-    case EPI_QKV: {
-      // swap orientation: A rows are features of the stacked [Q; K; V] projection.
-      const int Dh = e.head_dim, half = Dh >> 1;
-      const int nq = e.n_q_heads * Dh, nk = e.n_kv_heads * Dh;
-      for (int idx = etid; idx < total; idx += 128) {
-        const int a = idx & 127, b = idx >> 7;
-        const int f = m_tile * kBM + a;
-        const int t = n_tile * g.bn + col0 + b;
-        if (t >= e.n_tok || f >= e.n_feat) continue;
-        const int seq = t / e.rows_per_seq, i = t - seq * e.rows_per_seq;
-        const int pos = e.ctx_len[seq] + i;
-        const int d = f % Dh;
-        const float x = S[b * kSLD + a];
-        if (f < nq) {
-          const float xp = S[b * kSLD + (d < half ? a + half : a - half)];
-          store_out(e.out, e.out_bf16, static_cast<size_t>(t) * e.ld + f, rope_rot(e, pos, d, x, xp));
-        } else {
-          if (pos >= e.ncap) { report(g.dev_status, DFLASH_ERR_CAPACITY); continue; }
-          const bool is_k = f < nq + nk;
-          const int head = ((is_k ? f - nq : f - nq - nk)) / Dh;
-          float y = x;
-          if (is_k) y = rope_rot(e, pos, d, x, S[b * kSLD + (d < half ? a + half : a - half)]);
-          const size_t o =
-              ((static_cast<size_t>(e.layer) * e.max_batch + seq) * e.n_kv_heads + head) * e.ncap + pos;
-          store_out(is_k ? e.k_cache : e.v_cache, e.out_bf16, o * Dh + d, y);
-        }
-      }
-      break;
-    }
+    case EPI_QKV:
     case EPI_KV: {
       const int Dh = e.head_dim, half = Dh >> 1;
-      const int nk = e.n_kv_heads * Dh;
-      for (int idx = etid; idx < total; idx += 128) {
-        int a, b;
-        if (g.swap) { a = idx & 127; b = idx >> 7; } else { b = idx % cols; a = idx / cols; }
-        const int gf = g.swap ? m_tile * kBM + a : n_tile * g.bn + col0 + b;
-        const int r = g.swap ? n_tile * g.bn + col0 + b : m_tile * kBM + a;
-        if (r >= e.n_tok || gf >= e.n_feat) continue;
-        const int seq = r / e.rows_per_seq, t = r - seq * e.rows_per_seq;
-        const int nn = e.n_new[seq], base = e.ctx_len[seq];
-        if (t >= nn || base + nn > e.ncap - e.reserve) continue;
-        const int layer = gf / e.feat_per_layer, f = gf - layer * e.feat_per_layer;
-        const bool is_k = f < nk;
-        const int fk = is_k ? f : f - nk;
-        const int head = fk / Dh, d = fk % Dh;
-        const int pos = base + t;
-        const float x = S[b * kSLD + a];
-        float y = x;
-        if (is_k) {
-          const int pa = g.swap ? (d < half ? a + half : a - half) : a;
-          const int pb = g.swap ? b : (d < half ? b + half : b - half);
-          y = rope_rot(e, pos, d, x, S[pb * kSLD + pa]);
+      const int nq = e.n_q_heads * Dh, nk = e.n_kv_heads * Dh;
+      for (int base = etid; base < total; base += 128 * kEpiBatch) {
+        float y[kEpiBatch], cs[kEpiBatch], sn[kEpiBatch];
+        size_t o[kEpiBatch];
+        int kind[kEpiBatch];  // 0 skip, 1 q, 2 k, 3 v
+        int dd[kEpiBatch], pp[kEpiBatch];
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          const int idx = base + u * 128;
+          int a, b;
+          if (g.swap) { a = idx & 127; b = idx >> 7; } else { b = idx % cols; a = idx / cols; }
+          const int gf = g.swap ? m_tile * kBM + a : n_tile * g.bn + col0 + b;
+          const int x = tok_cols ? b : a;
+          const int tok = tok_cols ? n_tile * g.bn + col0 + b : m_tile * kBM + a;
+          kind[u] = 0;
+          dd[u] = 0;
+          pp[u] = 0;
+          o[u] = 0;
+          y[u] = 0.f;
+          if (idx < total && gf < e.n_feat) {
+            const int pos = ti->pos[x], seq = ti->seq[x];
+            int f = gf, layer = e.layer;
+            if (e.op == EPI_KV) {
+              layer = gf / e.feat_per_layer;
+              f = gf - layer * e.feat_per_layer + nq;   // position within the [Q; K; V] rows
+            }
+            const int d = f % Dh;
+            if (f < nq) {
+              kind[u] = 1;
+              o[u] = static_cast<size_t>(tok) * e.ld + f;
+            } else if (pos >= 0) {
+              const bool is_k = f < nq + nk;
+              const int head = (is_k ? f - nq : f - nq - nk) / Dh;
+              kind[u] = is_k ? 2 : 3;
+              o[u] = (((static_cast<size_t>(layer) * e.max_batch + seq) * e.n_kv_heads + head) * e.ncap + pos) * Dh + d;
+            }
+            if (kind[u] == 1 && tok >= e.n_tok) kind[u] = 0;
+            if (kind[u] != 0) {
+              dd[u] = d;
+              pp[u] = pos < 0 ? 0 : pos;
+              y[u] = S[b * kSLD + a];
+              if (kind[u] != 3 && e.rope_cos != nullptr) {
+                const int pa = g.swap ? (d < half ? a + half : a - half) : a;
+                const int pb = g.swap ? b : (d < half ? b + half : b - half);
+                cs[u] = S[pb * kSLD + pa];   // partner value, rotated below
+              }
+            }
+          }
         }
-        const size_t o = ((static_cast<size_t>(layer) * e.max_batch + seq) * e.n_kv_heads + head) * e.ncap + pos;
-        store_out(is_k ? e.k_cache : e.v_cache, e.out_bf16, o * Dh + d, y);
+        // table loads of the whole batch first, then the rotations and stores
+        float c[kEpiBatch], sv[kEpiBatch];
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          c[u] = 1.f;
+          sv[u] = 0.f;
+          if (kind[u] != 0 && kind[u] != 3 && e.rope_cos != nullptr) {
+            const int j = dd[u] < half ? dd[u] : dd[u] - half;
+            const size_t t = static_cast<size_t>(pp[u]) * half + j;
+            c[u] = e.rope_cos[t];
+            sv[u] = e.rope_sin[t];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kEpiBatch; ++u) {
+          if (kind[u] == 0) continue;
+          float val = y[u];
+          if (kind[u] != 3 && e.rope_cos != nullptr)
+            val = dd[u] < half ? y[u] * c[u] - cs[u] * sv[u] : y[u] * c[u] + cs[u] * sv[u];
+          void* dst = kind[u] == 1 ? e.out : (kind[u] == 2 ? e.k_cache : e.v_cache);
+          store_out(dst, e.out_bf16, o[u], val);
+        }
+        (void)sn;
       }
       break;
     }
@@ -206,8 +277,8 @@ struct SmemHeader {
   uint64_t accum;
   uint32_t tmem_base;
   int abort_flag;
-  int last_flag;
   int epi_ok;
+  TokInfo tok;
 };
 
 template <bool kTF32>
@@ -240,7 +311,6 @@ __global__ void __launch_bounds__(kGemmThreads)
     }
     mbar_init(smem_u32(&hdr->accum), 1);
     hdr->abort_flag = 0;
-    hdr->last_flag = 0;
     fence_mbar_init();
     fence_proxy_async();
   }
@@ -376,48 +446,65 @@ __global__ void __launch_bounds__(kGemmThreads)
             for (int i = 0; i < 16; ++i) S[(j + i) * kSLD + row] = v[i];
           }
           named_bar(1, 128);
-          apply_epilogue(g, S, c * kBM, cols, m_tile, n_tile, etid);
+          apply_epilogue(g, S, &hdr->tok, c * kBM, cols, m_tile, n_tile, etid);
           named_bar(1, 128);
         }
       } else {
-        const size_t tile_id = static_cast<size_t>(m_tile) * g.n_tiles + n_tile;
-        const size_t tile_elems = static_cast<size_t>(g.bn) * kBM;
-        float* part = g.partial + tile_id * g.splits * tile_elems;
-        float* mine = part + split * tile_elems;
+        // split-K: park this CTA's fp32 partial tile in its own shared memory
+        // ([col][row], the drained pipeline ring); the cluster reduces it below.
+        float* P = reinterpret_cast<float*>(tiles);
         for (int j = 0; j < g.bn; j += 16) {
           float v[16];
           tmem_ld16(t_lane + j, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) __stcg(&mine[(j + i) * kBM + row], v[i]);
-        }
-        __threadfence();
-        named_bar(1, 128);
-        if (etid == 0) {
-          const int prev = atomicAdd(&g.counters[tile_id], 1);
-          hdr->last_flag = (prev == g.splits - 1) ? 1 : 0;
-        }
-        named_bar(1, 128);
-        if (hdr->last_flag) {
-          __threadfence();
-          for (int c = 0; c < n_chunks; ++c) {
-            const int cols = min(kBM, g.bn - c * kBM);
-            for (int idx = etid; idx < cols * kBM; idx += 128) {
-              const int a = idx & 127, b = idx >> 7;
-              const size_t off = static_cast<size_t>(c * kBM + b) * kBM + a;
-              float acc = 0.f;
-              for (int s = 0; s < g.splits; ++s) acc += __ldcg(&part[s * tile_elems + off]);
-              S[b * kSLD + a] = acc;
-            }
-            named_bar(1, 128);
-            apply_epilogue(g, S, c * kBM, cols, m_tile, n_tile, etid);
-            named_bar(1, 128);
-          }
-          if (etid == 0) g.counters[tile_id] = 0;
+          for (int i = 0; i < 16; ++i) P[(j + i) * kBM + row] = v[i];
         }
       }
     }
     tc_fence_before();
+  }
+  if (g.splits > 1) {
+    // Split-K across the CTAs of this cluster (one cluster per output tile,
+    // cluster rank = split). After the barrier every partial is visible;
+    // CTA r reduces the token columns [c0, c1) of the tile by reading the
+    // partials of all splits through distributed shared memory, in ascending
+    // split order, then runs the epilogue on them. The second barrier keeps
+    // every partial alive until all peers have read it.
+    cluster_sync();
+    if (warp >= 2) {
+      const int etid = threadIdx.x - 64;
+      const uint32_t rank = cluster_ctarank();
+      const int valid = min(g.bn, g.n_rows - n_tile * g.bn);
+      const int per = (valid + g.splits - 1) / g.splits;
+      const int c0 = static_cast<int>(rank) * per, c1 = min(valid, c0 + per);
+      const uint32_t p_local = tiles_s;
+      float* S = reinterpret_cast<float*>(tiles + static_cast<size_t>(g.bn) * kBM * 4);
+      const bool ok = hdr->epi_ok != 0;
+      for (int cb = c0; cb < c1; cb += kBM) {
+        const int cols = min(kBM, c1 - cb);
+        if (ok) {
+          for (int it = etid; it < cols * (kBM / 4); it += 128) {
+            const int b = it / (kBM / 4), a = (it % (kBM / 4)) * 4;
+            const uint32_t off = static_cast<uint32_t>(((cb + b) * kBM + a) * 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int sp = 0; sp < g.splits; ++sp) {
+              const float4 v = ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(sp)));
+              acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            S[b * kSLD + a] = acc.x;
+            S[b * kSLD + a + 1] = acc.y;
+            S[b * kSLD + a + 2] = acc.z;
+            S[b * kSLD + a + 3] = acc.w;
+          }
+        }
+        named_bar(1, 128);
+        if (ok) apply_epilogue(g, S, &hdr->tok, cb, cols, m_tile, n_tile, etid);
+        named_bar(1, 128);
+      }
+    }
+    cluster_sync();
   }
   __syncthreads();
   if (warp == 1) {
@@ -481,26 +568,35 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   const size_t stage = 16384 + static_cast<size_t>(p.bn) * 128;
   const size_t staging = static_cast<size_t>(p.bn < kBM ? p.bn : kBM) * 129 * 4;
   const int ctas_per_sm = p.bn <= 64 ? 2 : 1;
-  const size_t budget = (ctas_per_sm == 2 ? 110 * 1024 : 222 * 1024) - 2048;
+  const size_t budget = (ctas_per_sm == 2 ? 110 * 1024 : 222 * 1024) - kSmemHeaderBytes;
   int stages = static_cast<int>(budget / stage);
   if (stages > 16) stages = 16;
   if (stages > KT && KT >= 2) stages = KT;
   if (stages < 2) stages = 2;
   while (static_cast<size_t>(stages) * stage < staging) ++stages;
   p.stages = stages;
-  p.smem_bytes = 2048 + static_cast<size_t>(stages) * stage;
+  p.smem_bytes = kSmemHeaderBytes + static_cast<size_t>(stages) * stage;
   int splits = 1;
   if (allow_split) {
+    // about two waves of CTAs over the machine; clusters hold at most 8 CTAs
     const int tiles = m_tiles * p.n_tiles;
-    const int target = num_sms * ctas_per_sm;
-    splits = target / (tiles > 0 ? tiles : 1);
+    const int target = 2 * num_sms * ctas_per_sm;
+    splits = (target + tiles / 2) / (tiles > 0 ? tiles : 1);
     if (splits > KT / 4) splits = KT / 4;
-    if (splits > 32) splits = 32;
+    if (splits > 8) splits = 8;
     if (splits < 1) splits = 1;
+    // the partial tile and the reduced column slice must fit in the ring
+    const size_t ring = static_cast<size_t>(stages) * stage;
+    while (splits > 1) {
+      const int per = (p.bn + splits - 1) / splits;
+      const size_t need = static_cast<size_t>(p.bn) * kBM * 4 + static_cast<size_t>(per < kBM ? per : kBM) * 129 * 4;
+      if (need <= ring) break;
+      if (splits < 8 && splits < KT / 4) ++splits; else { splits = 1; break; }
+    }
   }
   p.kt_per_split = (KT + splits - 1) / splits;
   p.splits = (KT + p.kt_per_split - 1) / p.kt_per_split;
-  p.partial_bytes = p.splits > 1 ? static_cast<size_t>(m_tiles) * p.n_tiles * p.splits * p.bn * kBM * 4 : 0;
+  p.partial_bytes = 0;
   return p;
 }
 
@@ -522,11 +618,22 @@ cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, cons
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (plan.splits > 1) {  // one cluster per output tile, spanning its splits
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = plan.splits;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, a_map, b_map, args, plan.stages);
 }
 

@@ -13,7 +13,6 @@ namespace dfl {
 constexpr int kBM = 128;        // MMA M: rows of the A operand per tile
 constexpr int kMaxBN = 512;     // B-operand rows per tile (two MMAs of <= 256)
 constexpr int kGemmThreads = 192;
-constexpr int kMaxGemmCounters = 8192;
 
 // Epilogue operations of the projection GEMM.
 enum EpiOp : int {
@@ -68,8 +67,6 @@ struct GemmArgs {
   int swap;           // 1: A rows are output features and B rows tokens; 0: the reverse
   int a_weights;      // 1: A is a weight (independent of earlier kernels): prefetch before PDL wait
   int tf32;           // 1: fp32 operands through kind::tf32
-  float* partial;     // split-K partial tiles
-  int* counters;      // split-K arrival counters (zero between launches)
   int* dev_status;
   Epi epi;
 };
@@ -100,15 +97,14 @@ struct AttnArgs {
   const void* v_cache;
   const int* ctx_len;     // [B]
   void* out;              // [B*R, Hq*Dh]
-  float* part;            // split partials
-  int* counters;          // [B*Hkv], zero between launches
   int* dev_status;
   int B, R, n_q_heads, n_kv_heads, head_dim, ncap, max_batch;
-  int splits, chunk;      // keys per split (multiple of 64); last split takes the rest
+  int splits, chunk;      // keys per split (multiple of 64); last split takes the rest;
+                          // the splits of one (sequence, KV head) form one cluster
   int bf16;
 };
-void plan_attention(int B, int R, int Hkv, int max_ctx, int ncap, int* splits, int* chunk);
-size_t attention_partial_bytes(int R, int Hq, int Hkv, int Dh);
+void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
+                    int* chunk);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
 
 // Small row kernels.

@@ -147,6 +147,20 @@ def test_chain_small_bf16_rope_off(dfl):
     run_chain(dfl, SMALL.replace(rope_theta=0.0, batch=1), [130])
 
 
+MEDIUM = synth.Workload("medium_bf16_L2", n_layers=2, d_target=512, n_taps=5, d_model=1024,
+                        n_q_heads=8, n_kv_heads=2, head_dim=128, d_ffn=2048, vocab=5000, gamma=16,
+                        dtype="bf16", batch=2, ctx=1000, seed=9)
+
+
+def test_chain_medium_bf16_split_k_clusters(dfl):
+    # K = 1024..2560 gives 4-8 k-splits per projection: exercises the cluster reduction
+    run_chain(dfl, MEDIUM, [1000, 77])
+
+
+def test_chain_medium_bf16_gamma_8(dfl):
+    run_chain(dfl, MEDIUM.replace(gamma=8, batch=3, ctx=400), [400, 1, 250])
+
+
 def test_chain_tiny_f32(dfl):
     wl = synth.WORKLOADS["tiny_f32_L1_N128"]
     run_chain(dfl, wl, [wl.ctx])
