@@ -157,9 +157,10 @@ class DraftCycle:
     def step(self, trace=None):
         d, wl = self.dfl, self.wl
         self.ctx_len.copy_(self.ctx0)
-        d.dflash_ctx_fuse(self.cfg, self.w, self.step_taps, self.h_new.view(-1, wl.d_model), self.ws)
+        d.dflash_ctx_fuse(self.cfg, self.w, self.step_taps, self.h_new.view(-1, wl.d_model), self.ws,
+                          trace=trace)
         d.dflash_kv_inject(self.cfg, self.w, self.h_new, self.n_new, self.ctx_len, self.k_cache,
-                           self.v_cache, self.status, self.ws)
+                           self.v_cache, self.status, self.ws, trace=trace)
         d.dflash_draft_block(self.cfg, self.w, self.anchor, self.ctx_len, self.max_ctx, self.k_cache,
                              self.v_cache, self.draft, self.status, self.ws, trace=trace)
         d.dflash_verify_accept(self.cfg, self.target, self.draft, self.tau, self.committed,
@@ -169,7 +170,7 @@ class DraftCycle:
         rec = self.dfl.TraceRecorder(256)
         self.step(trace=rec.struct)
         torch.cuda.synchronize()
-        return rec.struct.count + 4   # + fusion GEMM, fusion norm, injection GEMM, length advance
+        return rec.struct.count
 
 
 def time_steps(fn, steps: int, stream) -> float:

@@ -61,9 +61,9 @@ _SIGS = {
     "dflash_workspace_bytes": (_SZ, [ctypes.POINTER(Config), _I]),
     "dflash_workspace_init": (_I, [_P, _SZ, _P]),
     "dflash_ctx_fuse": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _I, _P,
-                             _P, _SZ, _P]),
+                             _P, _SZ, ctypes.POINTER(Trace), _P]),
     "dflash_kv_inject": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _I,
-                              _I, _P, _P, _P, _P, _P, _SZ, _P]),
+                              _I, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
     "dflash_draft_block": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P,
                                 _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                 ctypes.POINTER(Trace), _P]),
@@ -203,20 +203,24 @@ class Workspace:
         return self.buf.data_ptr()
 
 
-def dflash_ctx_fuse(cfg, w: Weights, taps, h_ctx, ws: Workspace, stream=None):
+def _tr(trace):
+    return ctypes.byref(trace) if trace is not None else None
+
+
+def dflash_ctx_fuse(cfg, w: Weights, taps, h_ctx, ws: Workspace, trace=None, stream=None):
     T = taps.shape[0] if taps is not None else 0
     _check("dflash_ctx_fuse", load().dflash_ctx_fuse(
         ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(taps), T, _ptr(h_ctx), ws.ptr, ws.nbytes,
-        _stream(stream)))
+        _tr(trace), _stream(stream)))
 
 
 def dflash_kv_inject(cfg, w: Weights, h_ctx, n_new, ctx_len, k_cache, v_cache, dev_status,
-                     ws: Workspace, stream=None):
+                     ws: Workspace, trace=None, stream=None):
     B, Tmax = h_ctx.shape[0], h_ctx.shape[1]
     _check("dflash_kv_inject", load().dflash_kv_inject(
         ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(h_ctx), _ptr(n_new), B, Tmax,
         _ptr(ctx_len), _ptr(k_cache), _ptr(v_cache), _ptr(dev_status), ws.ptr, ws.nbytes,
-        _stream(stream)))
+        _tr(trace), _stream(stream)))
 
 
 def dflash_draft_block(cfg, w: Weights, anchor, ctx_len, max_ctx_hint, k_cache, v_cache, draft,

@@ -12,6 +12,8 @@
 // tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with an online
 // softmax kept in registers (quad shuffles), and the last CTA of each
 // (sequence, KV head) merges the split partials in a fixed order.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,7 +21,7 @@ namespace dfl {
 namespace {
 
 constexpr int kKeyTile = 64;
-constexpr int kStagesKV = 3;
+constexpr int kStagesKV = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxAttnCluster = 16;  // split-KV CTAs of one (sequence, KV head): one cluster
 
@@ -120,13 +122,15 @@ __global__ void __launch_bounds__(256) attn_bf16_kernel(const AttnArgs p) {
       cp_async16(v_u + st * tile_bytes + swz<DH>(r, c), vg + off, bytes);
     }
   };
-  if (n_tiles > 0) load_tile(0);
-  cp_async_commit();
-  if (n_tiles > 1) load_tile(1);
-  cp_async_commit();
+  // the first kStagesKV - 1 tiles go out together with Q
+#pragma unroll
+  for (int t = 0; t < kStagesKV - 1; ++t) {
+    if (t < n_tiles) load_tile(t);
+    cp_async_commit();
+  }
 
   // Q fragments of this warp's 16 rows.
-  cp_async_wait<2>();
+  cp_async_wait<kStagesKV - 1>();
   __syncthreads();
   uint32_t qa[DH / 16][4];
   {
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(256) attn_bf16_kernel(const AttnArgs p) {
   const int t4 = lane & 3, g8 = lane >> 2;
 
   for (int t = 0; t < n_tiles; ++t) {
-    cp_async_wait<1>();
+    cp_async_wait<kStagesKV - 2>();
     __syncthreads();
     const int st = t % kStagesKV;
     const uint32_t ks = k_u + st * tile_bytes, vs = v_u + st * tile_bytes;
@@ -226,7 +230,7 @@ __global__ void __launch_bounds__(256) attn_bf16_kernel(const AttnArgs p) {
       }
     }
     __syncthreads();
-    if (t + 2 < n_tiles) load_tile(t + 2);
+    if (t + kStagesKV - 1 < n_tiles) load_tile(t + kStagesKV - 1);
     cp_async_commit();
   }
   cp_async_wait<0>();
@@ -284,41 +288,54 @@ __global__ void __launch_bounds__(256) attn_bf16_kernel(const AttnArgs p) {
   const int rank = static_cast<int>(cluster_ctarank());
   const int per = (n_q + p.splits - 1) / p.splits;
   const int r0 = rank * per, r1 = min(n_q, r0 + per);
+  const int nrows = r1 > r0 ? r1 - r0 : 0;
+  const int S = p.splits;
   const uint32_t po_u = smem_u32(po_s), ml_u = smem_u32(ml_s);
-  for (int qr = r0 + static_cast<int>(threadIdx.x); qr < r1; qr += blockDim.x) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp) {
-      float2 ml;
-      asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
-                   : "=f"(ml.x), "=f"(ml.y)
-                   : "r"(mapa_shared(ml_u + qr * 8, sp))
-                   : "memory");
-      w_loc[(qr - r0) * p.splits + sp] = ml.y > 0.f ? ml.x : -INFINITY;
-      w_loc[(qr - r0) * p.splits + sp + per * p.splits] = ml.y;
-      if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
-    float L = 0.f;
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const float m = w_loc[(qr - r0) * p.splits + sp];
-      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      w_loc[(qr - r0) * p.splits + sp] = w;
-      L += w_loc[(qr - r0) * p.splits + sp + per * p.splits] * w;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int sp = 0; sp < p.splits; ++sp) w_loc[(qr - r0) * p.splits + sp] *= inv;
+  float2* mls = reinterpret_cast<float2*>(w_loc + ((per * S + 1) & ~1));   // [row][split] (m, l)
+  // (m, l) of every (row, split) pair in parallel: one DSMEM load each
+  for (int pi = threadIdx.x; pi < nrows * S; pi += blockDim.x) {
+    const int qr = r0 + pi / S, sp = pi % S;
+    float2 ml;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(ml.x), "=f"(ml.y)
+                 : "r"(mapa_shared(ml_u + qr * 8, sp))
+                 : "memory");
+    mls[pi] = ml;
   }
   __syncthreads();
+  for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp)
+      if (mls[r * S + sp].y > 0.f) M = fmaxf(M, mls[r * S + sp].x);
+    float L = 0.f;
+    for (int sp = 0; sp < S; ++sp) {
+      const float2 ml = mls[r * S + sp];
+      const float w = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+      w_loc[r * S + sp] = w;
+      L += ml.y * w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int sp = 0; sp < S; ++sp) w_loc[r * S + sp] *= inv;
+  }
+  __syncthreads();
+  // O rows: every split's float4 is requested before any is summed; the sum
+  // runs in ascending split order.
   constexpr int D4 = DH / 4;
-  const int n_items = (r1 > r0 ? r1 - r0 : 0) * D4;
+  const int n_items = nrows * D4;
   for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
-    const int qr = r0 + it / D4, d = (it % D4) * 4;
+    const int r = it / D4, qr = r0 + r, d = (it % D4) * 4;
     const uint32_t off = po_u + static_cast<uint32_t>((qr * DH + d) * 4);
+    float4 v[kMaxAttnCluster];
+#pragma unroll
+    for (int sp = 0; sp < kMaxAttnCluster; ++sp)
+      if (sp < S) v[sp] = ld_dsmem_f4(mapa_shared(off, sp));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int sp = 0; sp < p.splits; ++sp) {
-      const float w = w_loc[(qr - r0) * p.splits + sp];
-      const float4 v = ld_dsmem_f4(mapa_shared(off, sp));
-      acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
+#pragma unroll
+    for (int sp = 0; sp < kMaxAttnCluster; ++sp) {
+      if (sp < S) {
+        const float w = w_loc[r * S + sp];
+        acc.x += v[sp].x * w; acc.y += v[sp].y * w; acc.z += v[sp].z * w; acc.w += v[sp].w * w;
+      }
     }
     __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(&out[out_index(qr, d)]);
     dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
@@ -408,6 +425,13 @@ void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap
   int sp = (n_keys + c - 1) / c;
   while (sp > kMaxAttnCluster) {
     c += kKeyTile;
+    sp = (n_keys + c - 1) / c;
+  }
+  if (const char* e = getenv("DFLASH_ATTN_SPLITS")) {   // tuning override
+    sp = atoi(e);
+    if (sp < 1) sp = 1;
+    if (sp > kMaxAttnCluster) sp = kMaxAttnCluster;
+    c = ((n_keys + sp - 1) / sp + kKeyTile - 1) / kKeyTile * kKeyTile;
     sp = (n_keys + c - 1) / c;
   }
   *splits = sp < 1 ? 1 : sp;

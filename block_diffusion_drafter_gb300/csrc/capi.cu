@@ -143,7 +143,8 @@ dflash_status dflash_check_config(const dflash_config* c) {
   if ((c->n_q_heads / c->n_kv_heads) * R > 128) return DFLASH_ERR_SHAPE;
   const int bk = c->dtype == DFLASH_BF16 ? 64 : 32;
   const long long kin = static_cast<long long>(c->n_taps) * c->d_target;
-  if (c->d_model % kBM || kin % bk || (c->n_q_heads * c->head_dim) % bk || c->d_ffn % 64)
+  if (c->d_model % kBM || c->d_model > 8192 || kin % bk || (c->n_q_heads * c->head_dim) % bk ||
+      c->d_ffn % 64)
     return DFLASH_ERR_SHAPE;
   if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % kBM) return DFLASH_ERR_SHAPE;
   if ((2 * c->n_kv_heads * c->head_dim) % kBM) return DFLASH_ERR_SHAPE;
@@ -257,6 +258,11 @@ Epi base_epi(const dflash_config* c) {
   return e;
 }
 
+bool trace_ok(const dflash_trace* t) {
+  return t == nullptr || (t->events != nullptr && t->kinds != nullptr && t->bytes != nullptr &&
+                          t->flops != nullptr && t->capacity >= 0);
+}
+
 bool rope_ok(const dflash_config* c, const dflash_weights* w) {
   if (c->rope_theta == 0.f) return true;
   return w->rope_cos != nullptr && w->rope_sin != nullptr && w->rope_positions >= c->ctx_capacity;
@@ -312,12 +318,14 @@ dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, fl
 }
 
 dflash_status dflash_ctx_fuse(const dflash_config* c, const dflash_weights* w, const void* taps, int T,
-                              void* h_ctx, void* ws, size_t ws_bytes, dflash_stream_t stream) {
+                              void* h_ctx, void* ws, size_t ws_bytes, dflash_trace* trace,
+                              dflash_stream_t stream) {
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
   if (w == nullptr || T < 0) return DFLASH_ERR_INVALID_ARG;
   if (T == 0) return DFLASH_OK;
-  if (taps == nullptr || h_ctx == nullptr || w->w_c == nullptr || w->g_c == nullptr)
+  if (taps == nullptr || h_ctx == nullptr || w->w_c == nullptr || w->g_c == nullptr ||
+      !trace_ok(trace))
     return DFLASH_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c);
   if (ws == nullptr || ws_bytes < L.fixed + static_cast<size_t>(T) * row_ss_bytes_per_row(c))
@@ -325,8 +333,7 @@ dflash_status dflash_ctx_fuse(const dflash_config* c, const dflash_weights* w, c
   if ((st = check_arch()) != DFLASH_OK) return st;
   const int es = elem_bytes(c), D = c->d_model, K = c->n_taps * c->d_target;
   Ctx cx{c, L, ws, reinterpret_cast<cudaStream_t>(stream), es, num_sms_of_current_device(), use_pdl(),
-         Tracer{nullptr, nullptr}};
-  cx.tr.s = cx.s;
+         Tracer{trace, reinterpret_cast<cudaStream_t>(stream)}};
   GemmArgs g{};
   CUtensorMap amap, bmap;
   GemmPlan plan;
@@ -359,22 +366,24 @@ dflash_status dflash_ctx_fuse(const dflash_config* c, const dflash_weights* w, c
   const double bytes = (static_cast<double>(T) * K + static_cast<double>(D) * K + static_cast<double>(T) * D) * es;
   if ((st = run_gemm(cx, g, amap, bmap, plan, bytes, 2.0 * T * D * static_cast<double>(K))) != DFLASH_OK)
     return st;
-  if (launch_fuse_norm(h_ctx, at<float>(ws, L.row_ss), D / kBM, w->g_c, T, D, c->rms_eps,
-                       c->dtype == DFLASH_BF16, cx.s, cx.pdl) != cudaSuccess)
-    return DFLASH_ERR_CUDA;
-  return DFLASH_OK;
+  cx.tr.before(DFLASH_K_NORM, 2.0 * T * D * es, 0);
+  const cudaError_t e = launch_fuse_norm(h_ctx, at<float>(ws, L.row_ss), D / kBM, w->g_c, T, D,
+                                         c->rms_eps, c->dtype == DFLASH_BF16, cx.s, cx.pdl);
+  cx.tr.after();
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
 dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, const void* h_ctx,
                                const int32_t* n_new, int B, int Tmax, int32_t* ctx_len, void* k_cache,
                                void* v_cache, int32_t* dev_status, void* ws, size_t ws_bytes,
-                               dflash_stream_t stream) {
+                               dflash_trace* trace, dflash_stream_t stream) {
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
   if (w == nullptr || B < 0 || B > c->max_batch || Tmax < 0) return DFLASH_ERR_INVALID_ARG;
   if (B == 0 || Tmax == 0) return DFLASH_OK;
   if (h_ctx == nullptr || n_new == nullptr || ctx_len == nullptr || k_cache == nullptr ||
-      v_cache == nullptr || dev_status == nullptr || w->w_qkv == nullptr || !rope_ok(c, w))
+      v_cache == nullptr || dev_status == nullptr || w->w_qkv == nullptr || !rope_ok(c, w) ||
+      !trace_ok(trace))
     return DFLASH_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c);
   if (ws == nullptr || ws_bytes < L.fixed) return DFLASH_ERR_WORKSPACE;
@@ -384,7 +393,7 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
   const int nqkv = (c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim;
   const int fpl = 2 * c->n_kv_heads * c->head_dim;
   Ctx cx{c, L, ws, reinterpret_cast<cudaStream_t>(stream), es, num_sms_of_current_device(), use_pdl(),
-         Tracer{nullptr, nullptr}};
+         Tracer{trace, reinterpret_cast<cudaStream_t>(stream)}};
   GemmArgs g{};
   CUtensorMap amap, bmap;
   GemmPlan plan;
@@ -429,10 +438,11 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
                         static_cast<double>(rows) * c->n_layers * fpl) * es;
   if ((st = run_gemm(cx, g, amap, bmap, plan, bytes, 2.0 * rows * c->n_layers * static_cast<double>(fpl) * D)) != DFLASH_OK)
     return st;
-  if (launch_kv_advance(ctx_len, n_new, B, Tmax, c->ctx_capacity, c->gamma + 1, dev_status, cx.s,
-                        cx.pdl) != cudaSuccess)
-    return DFLASH_ERR_CUDA;
-  return DFLASH_OK;
+  cx.tr.before(DFLASH_K_NORM, 12.0 * B, 0);
+  const cudaError_t e = launch_kv_advance(ctx_len, n_new, B, Tmax, c->ctx_capacity, c->gamma + 1,
+                                          dev_status, cx.s, cx.pdl);
+  cx.tr.after();
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
 }  // extern "C"
@@ -452,9 +462,7 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
       w->lm_head == nullptr || w->g_attn == nullptr || w->w_qkv == nullptr || w->w_o == nullptr ||
       w->g_ffn == nullptr || w->w_gateup == nullptr || w->w_down == nullptr || !rope_ok(c, w))
     return DFLASH_ERR_INVALID_ARG;
-  if (trace != nullptr && (trace->events == nullptr || trace->kinds == nullptr ||
-                           trace->bytes == nullptr || trace->flops == nullptr || trace->capacity < 0))
-    return DFLASH_ERR_INVALID_ARG;
+  if (!trace_ok(trace)) return DFLASH_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c);
   if (ws == nullptr || ws_bytes < L.fixed) return DFLASH_ERR_WORKSPACE;
   if ((st = check_arch()) != DFLASH_OK) return st;
@@ -632,9 +640,7 @@ dflash_status dflash_verify_accept(const dflash_config* c, const void* target_lo
   if (B < 1 || B > c->max_batch || target_logits == nullptr || draft == nullptr || tau == nullptr ||
       committed == nullptr || next_anchor == nullptr)
     return DFLASH_ERR_INVALID_ARG;
-  if (trace != nullptr && (trace->events == nullptr || trace->kinds == nullptr ||
-                           trace->bytes == nullptr || trace->flops == nullptr))
-    return DFLASH_ERR_INVALID_ARG;
+  if (!trace_ok(trace)) return DFLASH_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c);
   if (ws == nullptr || ws_bytes < L.fixed) return DFLASH_ERR_WORKSPACE;
   if ((st = check_arch()) != DFLASH_OK) return st;

@@ -15,6 +15,7 @@
 // meet in distributed shared memory and are summed in a fixed split order
 // (deterministic; no float atomics, no global partial buffers).
 #include <stdio.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -565,23 +566,33 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
     p.bn = cap1; p.n_sub = 1; p.n_tiles = (n_rows + cap1 - 1) / cap1;
   }
   p.m_tiles = m_tiles;
+  // Weight streaming wants many resident CTAs more than deep pipelines: a
+  // short ring (3 stages) leaves room for 3 CTAs per SM on the skinny
+  // shapes, whose prologue/epilogue then overlap other CTAs' streaming.
   const size_t stage = 16384 + static_cast<size_t>(p.bn) * 128;
   const size_t staging = static_cast<size_t>(p.bn < kBM ? p.bn : kBM) * 129 * 4;
-  const int ctas_per_sm = p.bn <= 64 ? 2 : 1;
-  const size_t budget = (ctas_per_sm == 2 ? 110 * 1024 : 222 * 1024) - kSmemHeaderBytes;
-  int stages = static_cast<int>(budget / stage);
+  int stages = p.bn <= 128 ? 3 : static_cast<int>((222 * 1024 - kSmemHeaderBytes) / stage);
+  if (const char* e = getenv("DFLASH_GEMM_STAGES")) stages = atoi(e);   // tuning override
   if (stages > 16) stages = 16;
   if (stages > KT && KT >= 2) stages = KT;
   if (stages < 2) stages = 2;
   while (static_cast<size_t>(stages) * stage < staging) ++stages;
   p.stages = stages;
   p.smem_bytes = kSmemHeaderBytes + static_cast<size_t>(stages) * stage;
+  // resident CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(p.bn)) tmem_cols <<= 1;
+  int ctas_per_sm = static_cast<int>(233472 / (p.smem_bytes + 1024));
+  if (ctas_per_sm > 4) ctas_per_sm = 4;
+  while (ctas_per_sm > 1 && ctas_per_sm * tmem_cols > 512) --ctas_per_sm;
+  if (ctas_per_sm < 1) ctas_per_sm = 1;
   int splits = 1;
   if (allow_split) {
-    // about two waves of CTAs over the machine; clusters hold at most 8 CTAs
+    // one wave over the resident slots; clusters hold at most 8 CTAs
     const int tiles = m_tiles * p.n_tiles;
-    const int target = 2 * num_sms * ctas_per_sm;
-    splits = (target + tiles / 2) / (tiles > 0 ? tiles : 1);
+    const int slots = num_sms * ctas_per_sm;
+    splits = slots / (tiles > 0 ? tiles : 1);
+    if (const char* e = getenv("DFLASH_GEMM_SPLITS")) splits = atoi(e);   // tuning override
     if (splits > KT / 4) splits = KT / 4;
     if (splits > 8) splits = 8;
     if (splits < 1) splits = 1;

@@ -42,6 +42,35 @@ __device__ __forceinline__ float block_sum256(float v, float* red) {
   return red[8];
 }
 
+// Loads of one row are issued up front (float4, up to kRowVec per thread) so a
+// row costs one memory latency rather than one per strided iteration.
+constexpr int kRowVec = 8;  // rows up to 256 threads x 8 float4 = 8192 floats
+
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+  *reinterpret_cast<float4*>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4 v) {
+  __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(dst);
+  d[0] = __floats2bfloat162_rn(v.x, v.y);
+  d[1] = __floats2bfloat162_rn(v.z, v.w);
+}
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* src);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* src) {
+  return *reinterpret_cast<const float4*>(src);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* src) {
+  const __nv_bfloat162* s = reinterpret_cast<const __nv_bfloat162*>(src);
+  const float2 a = __bfloat1622float2(s[0]), b = __bfloat1622float2(s[1]);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* anchor, int mask_id,
                                                     int R, int D, int V, float* h,
@@ -57,7 +86,18 @@ __global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* a
   }
   const T* src = embed + static_cast<size_t>(id) * D;
   float* dst = h + static_cast<size_t>(r) * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) dst[d] = to_f32(src[d]);
+  const int n4 = D / 4;
+  float4 v[kRowVec];
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int q = threadIdx.x + i * blockDim.x;
+    if (q < n4) v[i] = load4<T>(src + 4 * q);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int q = threadIdx.x + i * blockDim.x;
+    if (q < n4) reinterpret_cast<float4*>(dst)[q] = v[i];
+  }
   if (blockIdx.x == 0)
     for (int k = threadIdx.x; k < n_keys; k += blockDim.x) keys[k] = 0ull;
 }
@@ -71,13 +111,28 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const T* g
   const int r = blockIdx.x;
   const int src = mask_rows ? (r / gamma) * R + 1 + r % gamma : r;
   const float* xr = x + static_cast<size_t>(src) * D;
+  const int n4 = D / 4;
+  float4 v[kRowVec];
   float ss = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) ss += xr[d] * xr[d];
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int q = threadIdx.x + i * blockDim.x;
+    v[i] = q < n4 ? reinterpret_cast<const float4*>(xr)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
   ss = block_sum256(ss, red);
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
   T* o = out + static_cast<size_t>(r) * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x)
-    o[d] = from_f32<T>(to_f32(gain[d]) * xr[d] * inv);
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int q = threadIdx.x + i * blockDim.x;
+    if (q < n4) {
+      const float4 g = load4<T>(gain + 4 * q);
+      store4<T>(o + 4 * q, make_float4(g.x * v[i].x * inv, g.y * v[i].y * inv, g.z * v[i].z * inv,
+                                       g.w * v[i].w * inv));
+    }
+  }
 }
 
 template <typename T>
@@ -86,12 +141,26 @@ __global__ void __launch_bounds__(256) fuse_norm_kernel(T* h, const float* row_s
   pdl_launch_dependents();
   pdl_wait();
   const int r = blockIdx.x;
+  T* row = h + static_cast<size_t>(r) * D;
+  const int n4 = D / 4;
+  float4 v[kRowVec];
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int q = threadIdx.x + i * blockDim.x;
+    v[i] = q < n4 ? load4<T>(row + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float ss = 0.f;
   for (int s = 0; s < n_ss; ++s) ss += row_ss[static_cast<size_t>(r) * n_ss + s];
   const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
-  T* row = h + static_cast<size_t>(r) * D;
-  for (int d = threadIdx.x; d < D; d += blockDim.x)
-    row[d] = from_f32<T>(to_f32(gain[d]) * to_f32(row[d]) * inv);
+#pragma unroll
+  for (int i = 0; i < kRowVec; ++i) {
+    const int q = threadIdx.x + i * blockDim.x;
+    if (q < n4) {
+      const float4 g = load4<T>(gain + 4 * q);
+      store4<T>(row + 4 * q, make_float4(g.x * v[i].x * inv, g.y * v[i].y * inv, g.z * v[i].z * inv,
+                                         g.w * v[i].w * inv));
+    }
+  }
 }
 
 __global__ void argmax_finalize_kernel(unsigned long long* keys, int n, int32_t* draft) {

@@ -164,11 +164,13 @@ dflash_status dflash_workspace_init(void* ws, size_t ws_bytes,
  * taps:  [T, n_taps*Dt] -- row t is the n_taps tapped hidden states of the
  *        same token laid end to end in tap order (l1 first).
  * h_ctx: [T, D] output, cfg.dtype. T >= 0 (T == 0 launches nothing).
+ * trace: NULL or a dflash_trace (see above).
  * Errors: DFLASH_ERR_INVALID_ARG for null pointers with T > 0,
  *         DFLASH_ERR_WORKSPACE when T exceeds the workspace's max_rows. */
 dflash_status dflash_ctx_fuse(const dflash_config* cfg, const dflash_weights* w,
                               const void* taps, int T, void* h_ctx,
-                              void* ws, size_t ws_bytes, dflash_stream_t stream);
+                              void* ws, size_t ws_bytes, dflash_trace* trace,
+                              dflash_stream_t stream);
 
 /* KV injection, [P1] "KV Injection 메커니즘" (K_i, V_i equations) and
  * "추론 구조" (cached and reused across drafting iterations):
@@ -182,12 +184,14 @@ dflash_status dflash_ctx_fuse(const dflash_config* cfg, const dflash_weights* w,
  * k_cache, v_cache: [L, max_batch, Hkv, Ncap, Dh] (cfg.dtype).
  * dev_status: device int32; DFLASH_ERR_CAPACITY when ctx_len[b] + n_new[b]
  *   would exceed Ncap - R (the last R rows are reserved for the draft block);
- *   that sequence is then neither written nor advanced. */
+ *   that sequence is then neither written nor advanced.
+ * trace: NULL or a dflash_trace (see above). */
 dflash_status dflash_kv_inject(const dflash_config* cfg, const dflash_weights* w,
                                const void* h_ctx, const int32_t* n_new, int B,
                                int Tmax, int32_t* ctx_len, void* k_cache,
                                void* v_cache, int32_t* dev_status, void* ws,
-                               size_t ws_bytes, dflash_stream_t stream);
+                               size_t ws_bytes, dflash_trace* trace,
+                               dflash_stream_t stream);
 
 /* One-pass block drafting, [P4] §3.2-§3.3 and [P1] "추론 구조":
  *   h = Embed([anchor_b, m, ..., m])  (R rows at positions ctx_len[b]+0..gamma)

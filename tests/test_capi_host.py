@@ -106,11 +106,12 @@ def test_null_arguments_rejected_before_any_launch(lib):
     assert L.dflash_verify_accept(ctypes.byref(cfg), None, 0, None, 1, None, None, None, None, 0,
                                   None, None) == lib.ERR_INVALID_ARG
     assert L.dflash_kv_inject(ctypes.byref(cfg), ctypes.byref(w), None, None, 1, 4, None, None,
-                              None, None, None, 0, None) == lib.ERR_INVALID_ARG
+                              None, None, None, 0, None, None) == lib.ERR_INVALID_ARG
     # T == 0 and B == 0 are no-ops
-    assert L.dflash_ctx_fuse(ctypes.byref(cfg), ctypes.byref(w), None, 0, None, None, 0, None) == lib.OK
+    assert L.dflash_ctx_fuse(ctypes.byref(cfg), ctypes.byref(w), None, 0, None, None, 0, None,
+                             None) == lib.OK
     assert L.dflash_kv_inject(ctypes.byref(cfg), ctypes.byref(w), None, None, 0, 4, None, None,
-                              None, None, None, 0, None) == lib.OK
+                              None, None, None, 0, None, None) == lib.OK
     # batch beyond max_batch
     assert L.dflash_verify_accept(ctypes.byref(cfg), 1, 0, 1, cfg.max_batch + 1, 1, 1, 1, 1, 1,
                                   None, None) == lib.ERR_INVALID_ARG
