@@ -19,7 +19,7 @@ from . import _build
 
 F32, BF16 = 0, 1
 (OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_DTYPE, ERR_CAPACITY, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT,
- ERR_WORKSPACE, ERR_ALIGN) = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9
+ ERR_WORKSPACE, ERR_ALIGN, ERR_TOO_LARGE) = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10
 K_GEMM, K_ATTN, K_NORM, K_ARGMAX, K_VERIFY = range(5)
 
 
@@ -71,6 +71,7 @@ _SIGS = {
                                   ctypes.POINTER(Trace), _P]),
     "dflash_rope_tables": (_I, [ctypes.POINTER(Config), _I, _P, _P]),
     "dflash_linear": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
+    "dflash_verify_accept_noalloc": (_I, [ctypes.POINTER(Config), _P, _I, _P, _I, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -242,6 +243,17 @@ def dflash_verify_accept(cfg, target_logits, draft, tau, committed, next_anchor,
         ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), B, _ptr(tau), _ptr(committed),
         _ptr(next_anchor), ws.ptr, ws.nbytes,
         ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_verify_accept_noalloc(cfg, target_logits, draft, tau, committed, next_anchor,
+                                 stream=None):
+    """dflash_verify_accept with its scratch in the library's own device memory
+    (no workspace): for callers that cannot allocate device memory."""
+    dt = BF16 if target_logits.dtype == torch.bfloat16 else F32
+    B = target_logits.shape[0]
+    _check("dflash_verify_accept_noalloc", load().dflash_verify_accept_noalloc(
+        ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), B, _ptr(tau), _ptr(committed),
+        _ptr(next_anchor), _stream(stream)))
 
 
 def dflash_linear(x, w, y, ws: Workspace, stream=None):

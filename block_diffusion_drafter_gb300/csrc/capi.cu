@@ -12,8 +12,6 @@ using namespace dfl;
 
 namespace {
 
-constexpr int kNumSmsUpperBound = 192;
-
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline int elem_bytes(const dflash_config* c) { return c->dtype == DFLASH_BF16 ? 2 : 4; }
 inline int rows_per_block(const dflash_config* c) { return c->gamma + 1; }
@@ -55,6 +53,9 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+}  // namespace
+
+namespace dfl {
 dflash_status check_arch() {
   static int cached[64] = {};  // 0 unknown, 1 ok, 2 bad
   int dev = 0;
@@ -78,6 +79,9 @@ bool use_pdl() {
   }
   return v == 1;
 }
+}  // namespace dfl
+
+namespace {
 
 // Records trace events around one launch.
 struct Tracer {
@@ -123,6 +127,7 @@ const char* dflash_status_string(dflash_status s) {
     case DFLASH_ERR_TIMEOUT: return "device wait timed out";
     case DFLASH_ERR_WORKSPACE: return "workspace missing or too small";
     case DFLASH_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case DFLASH_ERR_TOO_LARGE: return "request beyond the fixed maximum size";
   }
   return "unknown status";
 }

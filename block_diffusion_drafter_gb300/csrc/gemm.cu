@@ -39,16 +39,6 @@ __device__ __forceinline__ void store_out(void* out, int bf16, size_t idx, float
     reinterpret_cast<float*>(out)[idx] = v;
 }
 
-// Rotate-half RoPE of element d of a head given its partner value.
-__device__ __forceinline__ float rope_rot(const Epi& e, int pos, int d, float x, float xp) {
-  if (e.rope_cos == nullptr) return x;
-  const int half = e.head_dim >> 1;
-  const int j = d < half ? d : d - half;
-  const size_t t = static_cast<size_t>(pos) * half + j;
-  const float c = e.rope_cos[t], s = e.rope_sin[t];
-  return d < half ? x * c - xp * s : x * c + xp * s;
-}
-
 // Applies the epilogue to one staged chunk: S[b * kSLD + a] holds C for
 // A-row a (0..127) and B-row col0 + b (0 <= b < cols) of tile (m_tile, n_tile).
 // Runs on the 128 epilogue threads (etid 0..127). Every op works in batches

@@ -127,6 +127,10 @@ cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, in
 cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t s, bool pdl);
 
 int num_sms_of_current_device();
+// DFLASH_ERR_ARCH unless the current device is sm_103 (cached per device).
+dflash_status check_arch();
+// Programmatic dependent launch on (default) unless DFLASH_PDL=0.
+bool use_pdl();
 int verify_chunks(int B, int R, int V);
 
 }  // namespace dfl

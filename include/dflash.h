@@ -61,7 +61,8 @@ typedef enum {
   DFLASH_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed            */
   DFLASH_ERR_TIMEOUT = -7,     /* device: a bounded wait ran out               */
   DFLASH_ERR_WORKSPACE = -8,   /* workspace missing or too small               */
-  DFLASH_ERR_ALIGN = -9        /* pointer not 16-byte aligned                  */
+  DFLASH_ERR_ALIGN = -9,       /* pointer not 16-byte aligned                  */
+  DFLASH_ERR_TOO_LARGE = -10   /* request beyond a fixed maximum size          */
 } dflash_status;
 
 typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
@@ -250,6 +251,30 @@ dflash_status dflash_rope_tables(const dflash_config* cfg, int n_pos,
  * drafting step; `ws` needs dflash_workspace_bytes of any valid config. */
 dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, float* y, int M,
                             int N, int K, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Greedy verification without a workspace, for callers that cannot allocate
+ * device memory: a serving engine whose memory pool already owns the GPU's
+ * memory, a plugin running inside another runtime's step, or a hot loop in
+ * which cudaMalloc's implicit device synchronisation is not acceptable. The
+ * pages have no counterpart; the computation is that of dflash_verify_accept
+ * and the results are identical.
+ * Scratch: a fixed array in the library's device memory (about 140 KB per GPU
+ * that loads the library, held until the process exits) instead of `ws`.
+ * Limits: B <= 1024 and B * (gamma + 1) <= 16384, else DFLASH_ERR_TOO_LARGE
+ * and nothing is launched.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Each call clears the part of the array it uses
+ * (cudaMemsetAsync on `stream`) and allocates nothing. All calls share the
+ * one array, which keeps the last call's contents: calls whose work overlaps
+ * on the GPU (different streams, or concurrent graphs) race on it and must be
+ * serialised by the caller. */
+dflash_status dflash_verify_accept_noalloc(const dflash_config* cfg,
+                                           const void* target_logits,
+                                           dflash_dtype logits_dtype,
+                                           const int32_t* draft, int B, int32_t* tau,
+                                           int32_t* committed, int32_t* next_anchor,
+                                           dflash_stream_t stream);
 
 #ifdef __cplusplus
 }

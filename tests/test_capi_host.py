@@ -33,7 +33,7 @@ def test_library_exports_every_header_function(lib):
 
 
 def test_status_strings(lib):
-    for s in range(0, -10, -1):
+    for s in range(0, -11, -1):
         assert lib.status_string(s) != "unknown status"
     assert lib.status_string(-99) == "unknown status"
 
