@@ -1,0 +1,477 @@
+// Context attention on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Every block row of every query head attends to all ctx_len[b] + R keys of
+// its KV head, with no mask (bidirectional inside the block): the K_i / V_i
+// equations of "KV Injection 메커니즘" in "DFlash: Block Diffusion for Flash
+// Speculative Decoding 논문 정리", and §3.2 of the marsggbo DFlash page.
+//
+// One CTA owns the G*R query rows of one (sequence, KV head) and a contiguous
+// slice of its keys. Per 128-key tile:
+//   S = Q K^T      tcgen05.mma, Q and K K-major in shared memory, S in TMEM
+//                  with one query row per TMEM lane (= per epilogue thread);
+//   softmax        row max / exp2 / row sum are thread-local; the running max
+//                  is raised lazily (O in TMEM is rescaled only when the max
+//                  grows by more than 2^8), P goes to shared memory as bf16;
+//   O += P V       tcgen05.mma with V as an MN-major operand, O in TMEM.
+// K and V tiles stream in by TMA through a 2-stage ring; warp 0 issues TMA,
+// warp 1 the MMAs, warps 2-9 run the softmax (two per TMEM lane quarter). The key slices of one
+// (sequence, KV head) form a thread-block cluster whose partial results are
+// merged through distributed shared memory.
+#include <stdlib.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dfl {
+namespace {
+
+constexpr int kTileKeys = 128;
+constexpr uint32_t kSub = 128 * 128;     // one 128-row x 128-byte swizzled sub-tile (16 KB)
+constexpr int kMaxCluster = 16;
+constexpr float kLog2eTc = 1.4426950408889634f;
+constexpr float kLazyRescale = 8.0f;     // log2 units the running max may lag behind
+
+struct AttnSmem {
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t q_full, s_full, s_free, p_full, o_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  float pmax[2][128];  // per-half row max of the current tile
+  float psum[2][128];  // per-half row sums at the end
+};
+
+constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// Byte offset of 16-byte chunk c (of a 128-byte row segment) in row r of a
+// 128-byte swizzled sub-tile.
+// 2^x by the hardware approximation (ex2.approx, relative error ~2^-22); its
+// result is rounded to bf16 for P anyway.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+// Bounded wait whose outcome is the same on every lane of the warp (the
+// warp-collective tcgen05 loads that follow need a converged warp).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity)) != 0;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                   const AttnArgs p) {
+  constexpr int NSUB = DH / 64;                      // 64-dim sub-tiles per head
+  constexpr uint32_t kQBytes = NSUB * kSub;
+  constexpr uint32_t kPBytes = 2 * kSub;             // 128 keys = two 64-key sub-tiles
+  constexpr uint32_t kKVBytes = 2 * NSUB * kSub;     // K then V of one tile
+  constexpr uint32_t kSCol = 0, kOCol = 128;         // TMEM columns of S and O
+  extern __shared__ uint8_t smem_raw[];
+  AttnSmem* hdr = reinterpret_cast<AttnSmem*>(smem_raw);
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + sizeof(AttnSmem) + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_s - raw_s);
+  const uint32_t q_s = base_s, p_s = q_s + kQBytes, kv_s = p_s + kPBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.n_q_heads / p.n_kv_heads;
+  const int n_q = G * p.R;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&hdr->kv_full[i]), 1);
+      mbar_init(smem_u32(&hdr->kv_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&hdr->q_full), kAttnThreads - 64);
+    mbar_init(smem_u32(&hdr->s_full), 1);
+    mbar_init(smem_u32(&hdr->s_free), kAttnThreads - 64);
+    mbar_init(smem_u32(&hdr->p_full), kAttnThreads - 64);
+    mbar_init(smem_u32(&hdr->o_done), 1);
+    hdr->abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&hdr->tmem_base), 256);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&k_map);
+    tma_prefetch_map(&v_map);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = hdr->tmem_base;
+  pdl_launch_dependents();
+  pdl_wait();
+
+  const int n_keys = p.ctx_len[b] + p.R;
+  const int k_begin = sp * p.chunk;
+  const int k_end = (sp == p.splits - 1) ? n_keys : min(n_keys, (sp + 1) * p.chunk);
+  const int nt = k_end > k_begin ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
+  const int slab = (p.layer * p.max_batch + b) * p.n_kv_heads + kvh;
+  volatile int* abort_flag = &hdr->abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first();
+      for (int t = 0; t < nt; ++t) {
+        const int st = t & 1, u = t >> 1;
+        if (u > 0 && !mbar_wait(smem_u32(&hdr->kv_empty[st]), (u - 1) & 1)) {
+          report(p.dev_status, DFLASH_ERR_TIMEOUT);
+          atomicExch(&hdr->abort_flag, 1);
+          break;
+        }
+        if (*abort_flag) break;
+        const uint32_t bar = smem_u32(&hdr->kv_full[st]);
+        const uint32_t kd = kv_s + st * kKVBytes, vd = kd + NSUB * kSub;
+        const int kb = k_begin + t * kTileKeys;
+        mbar_expect_tx(bar, kKVBytes);
+#pragma unroll
+        for (int j = 0; j < NSUB; ++j) {
+          tma_load_3d(kd + j * kSub, &k_map, bar, 64 * j, kb, slab, pol);
+          tma_load_3d(vd + j * kSub, &v_map, bar, 64 * j, kb, slab, pol);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = make_idesc(128, kTileKeys, kFmtBF16);
+      const uint32_t idesc_o = make_idesc(128, DH, kFmtBF16, 1);
+      bool ok = nt == 0 || mbar_wait(smem_u32(&hdr->q_full), 0);
+      for (int t = 0; ok && t < nt; ++t) {
+        const int st = t & 1, u = t >> 1;
+        ok = mbar_wait(smem_u32(&hdr->kv_full[st]), u & 1) &&
+             (t == 0 || mbar_wait(smem_u32(&hdr->s_free), (t - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kt = kv_s + st * kKVBytes, vt = kt + NSUB * kSub;
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
+          tc_mma_f16(tmem + kSCol, sw128_desc(q_s + off), sw128_desc(kt + off), idesc_s, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&hdr->s_full));
+        ok = mbar_wait(smem_u32(&hdr->p_full), t & 1);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+          const uint64_t a = sw128_desc(p_s + (ks >> 2) * kSub + (ks & 3) * 32);
+          const uint64_t bd = sw128_desc_mn(vt + ks * 2048, kSub, 1024);
+          tc_mma_f16(tmem + kOCol, a, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&hdr->o_done));
+        tc_commit(smem_u32(&hdr->kv_empty[st]));
+      }
+      if (!ok) {
+        report(p.dev_status, DFLASH_ERR_TIMEOUT);
+        atomicExch(&hdr->abort_flag, 1);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    // Warps 2..9: TMEM lane quarter (warp % 4) gives the query row; `half`
+    // picks keys 64*half..+63 of each S tile and columns of O.
+    const int q = (warp & 3) * 32 + lane;
+    const int half = (warp - 2) >> 2;
+    const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
+    const int gq = q / p.R, iq = q % p.R;
+    const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q);
+    const size_t row_off = (static_cast<size_t>(b) * p.R + iq) * hq_stride + static_cast<size_t>(kvh * G + gq) * DH;
+    constexpr int QC = DH / 8;          // 16-byte chunks of one Q row
+    // this thread's half of Q row q into the swizzled K-major tile (rows >= n_q zero)
+#pragma unroll
+    for (int c = half * (QC / 2); c < (half + 1) * (QC / 2); ++c) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (q < n_q) v = *reinterpret_cast<const uint4*>(qg + row_off + c * 8);
+      st_shared_v4(q_s + (c >> 3) * kSub + swz128(q, c & 7), v);
+    }
+    fence_proxy_async();
+    mbar_arrive(smem_u32(&hdr->q_full));
+
+    const float scale = rsqrtf(static_cast<float>(DH)) * kLog2eTc;
+    constexpr int HK = kTileKeys / 2;   // keys per half
+    constexpr int HO = DH / 2;          // O columns per half
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < nt; ++t) {
+      const int kb = k_begin + t * kTileKeys;
+      const int nvalid = min(kTileKeys, k_end - kb);
+      const int nv_half = min(HK, max(0, nvalid - half * HK));
+      if (!warp_wait(smem_u32(&hdr->s_full), t & 1)) { ok = false; break; }
+      tc_fence_after();
+      float sv[HK];
+#pragma unroll
+      for (int c0 = 0; c0 < HK; c0 += 16) tmem_ld16(t_row + kSCol + half * HK + c0, sv + c0);
+      tmem_ld_wait();
+      if (nv_half < HK) {
+#pragma unroll
+        for (int i = 0; i < HK; ++i)
+          if (i >= nv_half) sv[i] = -INFINITY;
+      }
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+#pragma unroll
+      for (int i = 8; i < HK; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // both halves of the row agree on its max
+      hdr->pmax[half][q] = mx;
+      named_bar(2 + (warp & 3), 64);
+      mx = fmaxf(hdr->pmax[0][q], hdr->pmax[1][q]) * scale;
+      const float m_new = fmaxf(m_run, mx);
+      const bool rescale = (m_run == -INFINITY) || (m_new > m_run + kLazyRescale);
+      const float m_use = rescale ? m_new : m_run;
+      // the previous P . V must be done before P is rewritten or O rescaled
+      if (t > 0) {
+        if (!warp_wait(smem_u32(&hdr->o_done), (t - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float alpha = rescale ? exp2_approx(m_run - m_new) : 1.f;
+          if (rescale) l_run *= alpha;
+          float ov[HO];
+#pragma unroll
+          for (int c0 = 0; c0 < HO; c0 += 16) tmem_ld16(t_row + kOCol + half * HO + c0, ov + c0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < HO; ++i) ov[i] *= alpha;
+#pragma unroll
+          for (int c0 = 0; c0 < HO; c0 += 16) tmem_st16(t_row + kOCol + half * HO + c0, ov + c0);
+          tmem_st_wait();
+        }
+      }
+      m_run = m_use;
+      if (nvalid < kTileKeys) {
+        // keys past the end of the slice: zero their V rows (cache rows beyond
+        // the context may hold anything, and 0 * NaN would poison O)
+        if (!warp_wait(smem_u32(&hdr->kv_full[t & 1]), (t >> 1) & 1)) { ok = false; break; }
+        if (q >= nvalid) {
+          const uint32_t vt = kv_s + (t & 1) * kKVBytes + NSUB * kSub;
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+            for (int c = half * 4; c < half * 4 + 4; ++c)
+              st_shared_v4(vt + j * kSub + q * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+        }
+      }
+      // P = 2^(s * scale - m) as bf16 into sub-tile `half` of the K-major P tile
+      float ls[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < HK / 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const float p0 = exp2_approx(fmaf(sv[c * 8 + i], scale, -m_use));
+          const float p1 = exp2_approx(fmaf(sv[c * 8 + i + 1], scale, -m_use));
+          ls[i] += p0;
+          ls[i + 1] += p1;
+          w[i >> 1] = pack2_bf16(p0, p1);
+        }
+        st_shared_v4(p_s + half * kSub + swz128(q, c), make_uint4(w[0], w[1], w[2], w[3]));
+      }
+      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&hdr->s_free));
+      mbar_arrive(smem_u32(&hdr->p_full));
+    }
+    if (ok && nt > 0) {
+      ok = warp_wait(smem_u32(&hdr->o_done), (nt - 1) & 1);
+      tc_fence_after();
+    }
+    if (!ok) {
+      report(p.dev_status, DFLASH_ERR_TIMEOUT);
+      atomicExch(&hdr->abort_flag, 1);
+    }
+    // row sum over both halves (same running max), in a fixed order
+    hdr->psum[half][q] = l_run;
+    named_bar(2 + (warp & 3), 64);
+    const float l_row = hdr->psum[0][q] + hdr->psum[1][q];
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    const bool have = ok && nt > 0;
+    float ov[HO];
+    if (have) {  // warp-uniform
+#pragma unroll
+      for (int c0 = 0; c0 < HO; c0 += 16) tmem_ld16(t_row + kOCol + half * HO + c0, ov + c0);
+      tmem_ld_wait();
+    }
+    if (p.splits == 1) {
+      if (have && q < n_q) {
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < HO; c0 += 8) {
+          uint4 w;
+          w.x = pack2_bf16(ov[c0] * inv, ov[c0 + 1] * inv);
+          w.y = pack2_bf16(ov[c0 + 2] * inv, ov[c0 + 3] * inv);
+          w.z = pack2_bf16(ov[c0 + 4] * inv, ov[c0 + 5] * inv);
+          w.w = pack2_bf16(ov[c0 + 6] * inv, ov[c0 + 7] * inv);
+          *reinterpret_cast<uint4*>(out + row_off + half * HO + c0) = w;
+        }
+      }
+    } else {
+      // park the unnormalised O row and (m, l) for the cluster merge
+      float* po = reinterpret_cast<float*>(base + (kv_s - base_s));
+      constexpr int PLD = DH + 4;
+#pragma unroll
+      for (int i = 0; i < HO; i += 4)
+        *reinterpret_cast<float4*>(&po[q * PLD + half * HO + i]) =
+            have ? make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (half == 0) {
+        float2* ml = reinterpret_cast<float2*>(po + 128 * PLD);
+        ml[q] = have ? make_float2(m_run, l_row) : make_float2(-INFINITY, 0.f);
+      }
+    }
+    tc_fence_before();
+  }
+
+  if (p.splits > 1) {
+    // Split-KV merge inside the cluster: CTA r merges a slice of the query
+    // rows, reading every split's O row and (m, l) through distributed shared
+    // memory in ascending split order, each weighted by 2^(m_s - M) / L.
+    cluster_sync();
+    constexpr int PLD = DH + 4;
+    float* po = reinterpret_cast<float*>(base + (kv_s - base_s));
+    float2* mlp = reinterpret_cast<float2*>(po + 128 * PLD);
+    const uint32_t po_u = kv_s, ml_u = smem_u32(mlp);
+    float* w_loc = reinterpret_cast<float*>(mlp + 128);
+    const int S = p.splits;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int per = (n_q + S - 1) / S;
+    const int r0 = rank * per, r1 = min(n_q, r0 + per);
+    const int nrows = r1 > r0 ? r1 - r0 : 0;
+    float2* mls = reinterpret_cast<float2*>(w_loc + ((per * S + 1) & ~1));
+    for (int pi = threadIdx.x; pi < nrows * S; pi += blockDim.x) {
+      const int qr = r0 + pi / S, s2 = pi % S;
+      float2 v;
+      asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                   : "=f"(v.x), "=f"(v.y)
+                   : "r"(mapa_shared(ml_u + qr * 8, s2))
+                   : "memory");
+      mls[pi] = v;
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < S; ++s2)
+        if (mls[r * S + s2].y > 0.f) M = fmaxf(M, mls[r * S + s2].x);
+      float L = 0.f;
+      for (int s2 = 0; s2 < S; ++s2) {
+        const float2 v = mls[r * S + s2];
+        const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
+        w_loc[r * S + s2] = w;
+        L += v.y * w;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int s2 = 0; s2 < S; ++s2) w_loc[r * S + s2] *= inv;
+    }
+    __syncthreads();
+    constexpr int D4 = DH / 4;
+    const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    for (int it = threadIdx.x; it < nrows * D4; it += blockDim.x) {
+      const int r = it / D4, qr = r0 + r, d = (it % D4) * 4;
+      const uint32_t off = po_u + static_cast<uint32_t>((qr * PLD + d) * 4);
+      float4 v[kMaxCluster];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxCluster; ++s2)
+        if (s2 < S) v[s2] = ld_dsmem_f4(mapa_shared(off, s2));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxCluster; ++s2) {
+        if (s2 < S) {
+          const float w = w_loc[r * S + s2];
+          acc.x += v[s2].x * w; acc.y += v[s2].y * w; acc.z += v[s2].z * w; acc.w += v[s2].w * w;
+        }
+      }
+      const int g = qr / p.R, i = qr % p.R;
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
+          out + (static_cast<size_t>(b) * p.R + i) * hq_stride + static_cast<size_t>(kvh * G + g) * DH + d);
+      dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
+      dst[1] = __floats2bfloat162_rn(acc.z, acc.w);
+    }
+    cluster_sync();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+}  // namespace dfl
+
+namespace dfl {
+
+cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl) {
+  if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
+  if ((a.n_q_heads / a.n_kv_heads) * a.R > 128 || a.splits > kMaxCluster) return cudaErrorInvalidValue;
+  // one tensor map per cache over all layers: [L * max_batch * Hkv][Ncap][Dh]
+  CUtensorMap km, vm;
+  const uint64_t slabs = static_cast<uint64_t>(a.n_layers) * a.max_batch * a.n_kv_heads;
+  if (!make_operand_map(&km, a.k_cache, 2, a.head_dim, a.ncap, slabs, kTileKeys) ||
+      !make_operand_map(&vm, a.v_cache, 2, a.head_dim, a.ncap, slabs, kTileKeys))
+    return cudaErrorInvalidValue;
+  const int nsub = a.head_dim / 64;
+  const size_t smem = sizeof(AttnSmem) + 1024 + static_cast<size_t>(nsub) * kSub + 2 * kSub +
+                      2 * static_cast<size_t>(2 * nsub) * kSub + 4096;  // + slack past the ring
+  void (*kern)(const CUtensorMap, const CUtensorMap, const AttnArgs) =
+      a.head_dim == 128 ? attn_tc_kernel<128> : attn_tc_kernel<64>;
+  static bool configured[2][64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  bool& done = configured[a.head_dim == 128][dev & 63];
+  if (!done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.splits, a.n_kv_heads, a.B);
+  cfg.blockDim = dim3(kAttnThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (a.splits > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = a.splits;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, km, vm, a);
+}
+
+}  // namespace dfl

@@ -487,7 +487,6 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
   void* act = at<void>(ws, L.act);
   void* z = at<void>(ws, L.z);
   unsigned long long* keys = at<unsigned long long>(ws, L.lm_keys);
-  const size_t layer_kv = static_cast<size_t>(c->max_batch) * c->n_kv_heads * c->ctx_capacity * c->head_dim * es;
   const double row_bytes = static_cast<double>(rows) * D * 4;
 
   // Skinny projection plans (tokens ride along as the MMA's N).
@@ -554,8 +553,10 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
     {
       AttnArgs a{};
       a.q = q;
-      a.k_cache = static_cast<const uint8_t*>(k_cache) + l * layer_kv;
-      a.v_cache = static_cast<const uint8_t*>(v_cache) + l * layer_kv;
+      a.k_cache = k_cache;
+      a.v_cache = v_cache;
+      a.layer = l;
+      a.n_layers = Lyr;
       a.ctx_len = ctx_len; a.out = ao;
       a.dev_status = dev_status;
       a.B = B; a.R = R; a.n_q_heads = c->n_q_heads; a.n_kv_heads = c->n_kv_heads;

@@ -145,6 +145,40 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// 32 lanes x 16 consecutive 32-bit columns from registers into TMEM.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Descriptor of an MN-major operand in the 128-byte swizzled layout: atoms of
+// 8 K-rows x 128 bytes (64 bf16 along M/N). The leading-dimension offset is
+// the byte stride between atoms along M/N, the stride offset the byte stride
+// between 8-row atoms along K (checked on the GPU against the oracle).
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t smem_addr, uint32_t mn_stride,
+                                                  uint32_t k_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((k_stride >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile stored in the
 // 128-byte swizzled layout that TMA writes with CU_TENSOR_MAP_SWIZZLE_128B:
@@ -165,10 +199,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 
 // Instruction descriptor of kind::f16 / kind::tf32: fp32 accumulator
 // (bits 4-5 = 1), A and B format (bits 7-9, 10-12: 0 f16, 1 bf16, 2 tf32),
-// both operands K-major (bits 15, 16 = 0), N >> 3 (bits 17-22),
-// M >> 4 (bits 24-28).
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n, uint32_t ab_format) {
-  return (1u << 4) | (ab_format << 7) | (ab_format << 10) |
+// A K-major (bit 15 = 0), B K-major or MN-major (bit 16), N >> 3
+// (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, uint32_t ab_format,
+                                                  uint32_t b_mn_major = 0) {
+  return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (b_mn_major << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 constexpr uint32_t kFmtBF16 = 1;

@@ -93,8 +93,9 @@ cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, cons
 // Attention over [injected context ; block] for one layer.
 struct AttnArgs {
   const void* q;          // [B*R, Hq*Dh]
-  const void* k_cache;    // layer slice [max_batch, Hkv, Ncap, Dh]
+  const void* k_cache;    // whole cache [L, max_batch, Hkv, Ncap, Dh]
   const void* v_cache;
+  int layer, n_layers;
   const int* ctx_len;     // [B]
   void* out;              // [B*R, Hq*Dh]
   int* dev_status;
@@ -106,6 +107,8 @@ struct AttnArgs {
 void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
                     int* chunk);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
+// bf16 path on tcgen05 (attention_tc.cu)
+cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl);
 
 // Small row kernels.
 cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
