@@ -44,8 +44,10 @@ WsLayout ws_layout(const dflash_config* c) {
   return L;
 }
 
+// Per context row of a fusion call: fp32 u = W_c x (D floats) followed, in a
+// second region, by its D/128 partial sums of squares.
 size_t row_ss_bytes_per_row(const dflash_config* c) {
-  return static_cast<size_t>(c->d_model / kBM) * 4;
+  return static_cast<size_t>(c->d_model) * 4 + static_cast<size_t>(c->d_model / kBM) * 4;
 }
 
 template <typename T>
@@ -360,20 +362,24 @@ dflash_status dflash_ctx_fuse(const dflash_config* c, const dflash_weights* w, c
   g.m_rows = swap ? D : T;
   g.n_rows = swap ? T : D;
   g.dev_status = nullptr;
+  // u = W_c x stays fp32 in the workspace; the norm pass rounds once to cfg.dtype
+  float* u32 = at<float>(ws, L.row_ss);
+  float* row_ss = u32 + static_cast<size_t>(T) * D;
   g.epi = base_epi(c);
   g.epi.op = EPI_FUSE;
-  g.epi.out = h_ctx;
+  g.epi.out = u32;
+  g.epi.out_bf16 = 0;
   g.epi.ld = D;
   g.epi.n_tok = T;
   g.epi.n_feat = D;
-  g.epi.row_ss = at<float>(ws, L.row_ss);
+  g.epi.row_ss = row_ss;
   g.epi.n_ss = D / kBM;
   const double bytes = (static_cast<double>(T) * K + static_cast<double>(D) * K + static_cast<double>(T) * D) * es;
   if ((st = run_gemm(cx, g, amap, bmap, plan, bytes, 2.0 * T * D * static_cast<double>(K))) != DFLASH_OK)
     return st;
   cx.tr.before(DFLASH_K_NORM, 2.0 * T * D * es, 0);
-  const cudaError_t e = launch_fuse_norm(h_ctx, at<float>(ws, L.row_ss), D / kBM, w->g_c, T, D,
-                                         c->rms_eps, c->dtype == DFLASH_BF16, cx.s, cx.pdl);
+  const cudaError_t e = launch_fuse_norm(u32, h_ctx, row_ss, D / kBM, w->g_c, T, D, c->rms_eps,
+                                         c->dtype == DFLASH_BF16, cx.s, cx.pdl);
   cx.tr.after();
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }

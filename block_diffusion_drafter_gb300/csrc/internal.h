@@ -118,8 +118,9 @@ cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int 
 // (r / gamma) * R + 1 + r % gamma (the mask rows of each block).
 cudaError_t launch_rmsnorm(const float* x, const void* gain, void* out, int rows, int D, float eps,
                            int bf16, int mask_rows, int gamma, int R, cudaStream_t s, bool pdl);
-cudaError_t launch_fuse_norm(void* h, const float* row_ss, int n_ss, const void* gain, int T,
-                             int D, float eps, int bf16, cudaStream_t s, bool pdl);
+// h[t] = gain * u[t] / sqrt(sum(row_ss[t]) / D + eps), u fp32, h in cfg dtype.
+cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
+                             int T, int D, float eps, int bf16, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int32_t* draft,
                                    cudaStream_t s, bool pdl);
 cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,

@@ -136,18 +136,19 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const T* g
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) fuse_norm_kernel(T* h, const float* row_ss, int n_ss,
-                                                        const T* gain, int D, float eps) {
+__global__ void __launch_bounds__(256) fuse_norm_kernel(const float* u, T* h, const float* row_ss,
+                                                        int n_ss, const T* gain, int D, float eps) {
   pdl_launch_dependents();
   pdl_wait();
   const int r = blockIdx.x;
+  const float* ur = u + static_cast<size_t>(r) * D;
   T* row = h + static_cast<size_t>(r) * D;
   const int n4 = D / 4;
   float4 v[kRowVec];
 #pragma unroll
   for (int i = 0; i < kRowVec; ++i) {
     const int q = threadIdx.x + i * blockDim.x;
-    v[i] = q < n4 ? load4<T>(row + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[i] = q < n4 ? reinterpret_cast<const float4*>(ur)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float ss = 0.f;
   for (int s = 0; s < n_ss; ++s) ss += row_ss[static_cast<size_t>(r) * n_ss + s];
@@ -289,13 +290,13 @@ cudaError_t launch_rmsnorm(const float* x, const void* gain, void* out, int rows
                    mask_rows, gamma, R);
 }
 
-cudaError_t launch_fuse_norm(void* h, const float* row_ss, int n_ss, const void* gain, int T, int D,
-                             float eps, int bf16, cudaStream_t s, bool pdl) {
+cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
+                             int T, int D, float eps, int bf16, cudaStream_t s, bool pdl) {
   if (bf16)
-    return launch_ex(fuse_norm_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, s, pdl,
+    return launch_ex(fuse_norm_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, s, pdl, u,
                      reinterpret_cast<__nv_bfloat16*>(h), row_ss, n_ss,
                      reinterpret_cast<const __nv_bfloat16*>(gain), D, eps);
-  return launch_ex(fuse_norm_kernel<float>, dim3(T), dim3(256), 0, s, pdl, reinterpret_cast<float*>(h),
+  return launch_ex(fuse_norm_kernel<float>, dim3(T), dim3(256), 0, s, pdl, u, reinterpret_cast<float*>(h),
                    row_ss, n_ss, reinterpret_cast<const float*>(gain), D, eps);
 }
 

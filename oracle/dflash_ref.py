@@ -121,17 +121,18 @@ def split_qkv(cfg: Cfg, w_qkv_layer):
     return w[:nq], w[nq:nq + nk], w[nq + nk:nq + 2 * nk]
 
 
-def ctx_kv(cfg: Cfg, w_qkv_layer, h_ctx, pos0: int):
+def ctx_kv(cfg: Cfg, w_qkv_layer, h_ctx, pos0: int, positions=None):
     """Injected context entries of one layer, [P1] "KV Injection 메커니즘":
     the first (context) part of K_i = [W_i^K H_t ; W_i^K H_d]_seq and of V_i.
-    Row t sits at absolute position pos0 + t; RoPE applies to K (reading).
-    Returns K, V as [Hkv, T, Dh]."""
+    Row t sits at absolute position pos0 + t (or positions[t] when given);
+    RoPE applies to K (reading). Returns K, V as [Hkv, T, Dh]."""
     _, wk, wv = split_qkv(cfg, w_qkv_layer)
     h = f64(h_ctx)
     T = h.shape[0]
     k = linear(h, wk).reshape(T, cfg.n_kv_heads, cfg.head_dim)
     v = linear(h, wv).reshape(T, cfg.n_kv_heads, cfg.head_dim)
-    k = rope(k, pos0 + np.arange(T), cfg.rope_theta)
+    pos = pos0 + np.arange(T) if positions is None else np.asarray(positions)
+    k = rope(k, pos, cfg.rope_theta)
     return k.transpose(1, 0, 2), v.transpose(1, 0, 2)
 
 

@@ -229,10 +229,10 @@ def loop_plan(wl: Workload, cycle: int, p_agree: float = 0.8):
     return agree, offset
 
 
-def loop_target_logits(wl: Workload, cycle: int, draft: torch.Tensor,
-                       anchor_tokens: torch.Tensor | None = None,
+def loop_target_logits(wl: Workload, cycle: int, draft: torch.Tensor, seqs=None,
                        dtype=torch.float32) -> torch.Tensor:
-    """[B, R, V] synthetic target logits for one loop cycle.
+    """[len(seqs), R, V] synthetic target logits for one loop cycle (all B
+    sequences when seqs is None; draft holds the drafts of those sequences).
 
     N(0,1) noise, then the "intended" token of row j gets max(row) + 1 so it
     is the unique argmax: draft[b, j] where loop_plan says agree, otherwise
@@ -240,11 +240,12 @@ def loop_target_logits(wl: Workload, cycle: int, draft: torch.Tensor,
     only integer indexing and one max per row, on draft's device."""
     dev = draft.device
     B, R, V = wl.batch, wl.rows, wl.vocab
-    noise = normal((B, R, V), wl.seed, f"loop_noise/{cycle}", dev)
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    noise = normal((B, R, V), wl.seed, f"loop_noise/{cycle}", dev)[seqs]
     agree, offset = loop_plan(wl, cycle)
-    agree_t = torch.as_tensor(agree, device=dev)
-    offset_t = torch.as_tensor(offset, device=dev)
-    base = torch.zeros((B, R), dtype=torch.int64, device=dev)
+    agree_t = torch.as_tensor(agree[seqs], device=dev)
+    offset_t = torch.as_tensor(offset[seqs], device=dev)
+    base = torch.zeros((len(seqs), R), dtype=torch.int64, device=dev)
     base[:, : R - 1] = draft.to(torch.int64)
     other = (base + offset_t) % V
     intended = torch.where(agree_t, base, other)
