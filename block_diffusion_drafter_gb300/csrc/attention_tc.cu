@@ -323,12 +323,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
 #pragma unroll
         for (int c0 = 0; c0 < HO; c0 += 8) {
+          float x[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] = ov[c0 + i] * inv;
           uint4 w;
-          w.x = pack2_bf16(ov[c0] * inv, ov[c0 + 1] * inv);
-          w.y = pack2_bf16(ov[c0 + 2] * inv, ov[c0 + 3] * inv);
-          w.z = pack2_bf16(ov[c0 + 4] * inv, ov[c0 + 5] * inv);
-          w.w = pack2_bf16(ov[c0 + 6] * inv, ov[c0 + 7] * inv);
+          w.x = pack2_bf16(x[0], x[1]); w.y = pack2_bf16(x[2], x[3]);
+          w.z = pack2_bf16(x[4], x[5]); w.w = pack2_bf16(x[6], x[7]);
           *reinterpret_cast<uint4*>(out + row_off + half * HO + c0) = w;
+          if (p.out_lo_off) {
+            const __nv_bfloat162* hw = reinterpret_cast<const __nv_bfloat162*>(&w);
+            uint4 lw;
+            uint32_t* l = reinterpret_cast<uint32_t*>(&lw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 hf = __bfloat1622float2(hw[i]);
+              l[i] = pack2_bf16(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
+            }
+            *reinterpret_cast<uint4*>(out + p.out_lo_off + row_off + half * HO + c0) = lw;
+          }
         }
       }
     } else {
@@ -407,10 +419,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       const int g = qr / p.R, i = qr % p.R;
-      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
-          out + (static_cast<size_t>(b) * p.R + i) * hq_stride + static_cast<size_t>(kvh * G + g) * DH + d);
-      dst[0] = __floats2bfloat162_rn(acc.x, acc.y);
-      dst[1] = __floats2bfloat162_rn(acc.z, acc.w);
+      const size_t oi = (static_cast<size_t>(b) * p.R + i) * hq_stride + static_cast<size_t>(kvh * G + g) * DH + d;
+      store_hilo(out, oi, p.out_lo_off, acc.x);
+      store_hilo(out, oi + 1, p.out_lo_off, acc.y);
+      store_hilo(out, oi + 2, p.out_lo_off, acc.z);
+      store_hilo(out, oi + 3, p.out_lo_off, acc.w);
     }
     cluster_sync();
   }

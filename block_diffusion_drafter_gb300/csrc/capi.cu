@@ -17,7 +17,7 @@ inline int elem_bytes(const dflash_config* c) { return c->dtype == DFLASH_BF16 ?
 inline int rows_per_block(const dflash_config* c) { return c->gamma + 1; }
 
 struct WsLayout {
-  size_t h, xn, q, attn_o, act, z, lm_keys, v_keys, v_count;
+  size_t h, xn, q, attn_o, act, z, ss, lm_keys, v_keys, v_count;
   size_t row_ss;
   size_t fixed;  // bytes before row_ss
 };
@@ -30,12 +30,16 @@ WsLayout ws_layout(const dflash_config* c) {
   const size_t D = c->d_model, HD = static_cast<size_t>(c->n_q_heads) * c->head_dim;
   size_t off = 0;
   auto take = [&](size_t bytes) { const size_t o = off; off = align256(off + bytes); return o; };
+  // bf16 models keep the activations that feed a projection as hi + lo bf16
+  // halves (two row blocks), fp32 models as one block
+  const size_t parts = c->dtype == DFLASH_BF16 ? 2 : 1;
   L.h = take(rows * D * 4);
-  L.xn = take(rows * D * es);
+  L.xn = take(parts * rows * D * es);
   L.q = take(rows * HD * es);
-  L.attn_o = take(rows * HD * es);
-  L.act = take(rows * static_cast<size_t>(c->d_ffn) * es);
-  L.z = take(static_cast<size_t>(c->max_batch) * c->gamma * D * es);
+  L.attn_o = take(parts * rows * HD * es);
+  L.act = take(parts * rows * static_cast<size_t>(c->d_ffn) * es);
+  L.z = take(parts * static_cast<size_t>(c->max_batch) * c->gamma * D * es);
+  L.ss = take(rows * (D / kBM) * 4);
   L.lm_keys = take(static_cast<size_t>(c->max_batch) * c->gamma * 8);
   L.v_keys = take(rows * 8);
   L.v_count = take(static_cast<size_t>(c->max_batch) * 4);
@@ -495,32 +499,82 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
   unsigned long long* keys = at<unsigned long long>(ws, L.lm_keys);
   const double row_bytes = static_cast<double>(rows) * D * 4;
 
-  // Skinny projection plans (tokens ride along as the MMA's N).
-  const GemmPlan p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true);
-  const GemmPlan p_o = plan_gemm(D / kBM, rows, HD, es, cx.sms, true);
-  const GemmPlan p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true);
-  const GemmPlan p_dn = plan_gemm(D / kBM, rows, F, es, cx.sms, true);
-  const GemmPlan p_lm = plan_gemm((V + kBM - 1) / kBM, nmask, D, es, cx.sms, false);
+  // Skinny projection plans (tokens ride along as the MMA's N). bf16 models
+  // feed each projection hi and lo halves of its activation (split = true).
+  const bool split = bf16 != 0;
+  const int rows_max = c->max_batch * R, nmask_max = c->max_batch * c->gamma;
+  const int parts = split ? 2 : 1;
+  GemmPlan p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, kMaxBN, split);
+  const GemmPlan p_o = plan_gemm(D / kBM, rows, HD, es, cx.sms, true, kMaxBN, split);
+  GemmPlan p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, kMaxBN, split);
+  if (p_qkv.b_split != p_gu.b_split) {  // both read the same normed activations
+    p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, kMaxBN, false);
+    p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, kMaxBN, false);
+  }
+  const GemmPlan p_dn = plan_gemm(D / kBM, rows, F, es, cx.sms, true, kMaxBN, split);
+  const GemmPlan p_lm = plan_gemm((V + kBM - 1) / kBM, nmask, D, es, cx.sms, false, kMaxBN, split);
 
+  // B boxes bring the valid token rows alone (hi and lo rows when the plan
+  // packs split operands) when one box spans the tile
+  auto box_of = [](const GemmPlan& p, int n) {
+    return p.b_split ? 2 * n : (p.n_sub == 1 && p.n_tiles == 1 ? n : p.bn / p.n_sub);
+  };
   CUtensorMap m_qkv, m_o, m_gu, m_dn, m_lm, m_xn, m_ao, m_act, m_z;
   bool ok = make_operand_map(&m_qkv, w->w_qkv, es, D, nqkv, Lyr, kBM) &&
             make_operand_map(&m_o, w->w_o, es, HD, D, Lyr, kBM) &&
             make_operand_map(&m_gu, w->w_gateup, es, D, 2 * F, Lyr, 64) &&
             make_operand_map(&m_dn, w->w_down, es, F, D, Lyr, kBM) &&
             make_operand_map(&m_lm, w->lm_head, es, D, V, 1, kBM) &&
-            make_operand_map(&m_xn, xn, es, D, rows, 1, p_qkv.bn / p_qkv.n_sub) &&
-            make_operand_map(&m_ao, ao, es, HD, rows, 1, p_o.bn / p_o.n_sub) &&
-            make_operand_map(&m_act, act, es, F, rows, 1, p_dn.bn / p_dn.n_sub) &&
-            make_operand_map(&m_z, z, es, D, nmask, 1, p_lm.bn / p_lm.n_sub);
+            make_operand_map(&m_xn, xn, es, D, parts * rows_max, 1, box_of(p_qkv, rows)) &&
+            make_operand_map(&m_ao, ao, es, HD, parts * rows_max, 1, box_of(p_o, rows)) &&
+            make_operand_map(&m_act, act, es, F, parts * rows_max, 1, box_of(p_dn, rows)) &&
+            make_operand_map(&m_z, z, es, D, parts * nmask_max, 1, box_of(p_lm, nmask));
   if (!ok) return DFLASH_ERR_ALIGN;
   CUtensorMap m_xn_gu;  // same buffer, box of the gate|up plan
-  if (!make_operand_map(&m_xn_gu, xn, es, D, rows, 1, p_gu.bn / p_gu.n_sub)) return DFLASH_ERR_ALIGN;
+  if (!make_operand_map(&m_xn_gu, xn, es, D, parts * rows_max, 1, box_of(p_gu, rows)))
+    return DFLASH_ERR_ALIGN;
+  // Each activation buffer carries lo = x - bf16(x) rows right after its hi
+  // rows when its consuming projection takes split operands (the planner
+  // decides per shape), so that one box brings both.
+  const bool s_xn = p_qkv.b_split && p_gu.b_split, s_ao = p_o.b_split, s_act = p_dn.b_split,
+             s_z = p_lm.b_split;
+  const size_t xn_lo = s_xn ? static_cast<size_t>(rows) * D : 0;
+  const size_t ao_lo = s_ao ? static_cast<size_t>(rows) * HD : 0;
+  const size_t act_lo = s_act ? static_cast<size_t>(rows) * F : 0;
+  const size_t z_lo = s_z ? static_cast<size_t>(nmask) * D : 0;
+  auto pack_of = [&](bool on, int n) { return on ? n : 0; };
 
   auto fail = [](cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA; };
 
-  cx.tr.before(DFLASH_K_NORM, row_bytes, 0);
-  st = fail(launch_embed(w->embed, anchor, c->mask_token_id, B, R, D, V, bf16, h, keys, nmask,
-                         dev_status, cx.s, cx.pdl));
+  float* ss = at<float>(ws, L.ss);
+  const int n_ss = D / kBM;
+  // RMSNorm is folded into the projections: the producer of h writes g (.) h and
+  // per-token sums of squares; the consuming GEMM scales by rstd per token.
+  auto fold_in = [&](Epi& e) {
+    e.ss_in = ss;
+    e.n_ss = n_ss;
+    e.d_model = D;
+    e.eps = c->rms_eps;
+  };
+  auto fold_out = [&](Epi& e, void* xg, const void* gain, int mask_rows) {
+    e.xg_out = xg;
+    e.lo_off = mask_rows ? z_lo : xn_lo;
+    e.xg_gain = gain;
+    e.xg_bf16 = bf16;
+    e.ss_out = ss;
+    e.n_ss = n_ss;
+    e.d_model = D;
+    e.xg_mask_rows = mask_rows;
+    e.gamma = c->gamma;
+    e.rows_per_seq = R;
+  };
+  auto gain_of = [&](const void* g, int l) {
+    return static_cast<const void*>(static_cast<const uint8_t*>(g) + static_cast<size_t>(l) * D * es);
+  };
+
+  cx.tr.before(DFLASH_K_NORM, row_bytes + static_cast<double>(rows) * D * es, 0);
+  st = fail(launch_embed(w->embed, anchor, c->mask_token_id, B, R, D, V, bf16, h, gain_of(w->g_attn, 0),
+                         xn, xn_lo, ss, keys, nmask, dev_status, cx.s, cx.pdl));
   cx.tr.after();
   if (st != DFLASH_OK) return st;
   if (layer_dump_opt != nullptr &&
@@ -532,17 +586,11 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
                  &a_splits, &a_chunk);
 
   for (int l = 0; l < Lyr; ++l) {
-    const size_t gain_off = static_cast<size_t>(l) * D * es;
-    // attention input norm
-    cx.tr.before(DFLASH_K_NORM, row_bytes + static_cast<double>(rows) * D * es, 0);
-    st = fail(launch_rmsnorm(h, static_cast<const uint8_t*>(w->g_attn) + gain_off, xn, rows, D,
-                             c->rms_eps, bf16, 0, c->gamma, R, cx.s, cx.pdl));
-    cx.tr.after();
-    if (st != DFLASH_OK) return st;
-    // Q/K/V projection; RoPE; block K/V into the cache scratch rows
+    // Q/K/V projection of RMSNorm(h): RoPE; block K/V into the cache scratch rows
     {
       GemmArgs g{};
       g.k = D; g.m_rows = nqkv; g.n_rows = rows; g.swap = 1; g.a_weights = 1; g.a_z0 = l;
+      g.b_pack = pack_of(s_xn, rows); g.b_box_rows = box_of(p_qkv, rows);
       g.dev_status = dev_status;
       g.epi = base_epi(c);
       g.epi.op = EPI_QKV; g.epi.out = q; g.epi.ld = HD; g.epi.n_tok = rows; g.epi.n_feat = nqkv;
@@ -551,6 +599,7 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
       g.epi.rope_cos = c->rope_theta > 0.f ? w->rope_cos : nullptr;
       g.epi.rope_sin = c->rope_theta > 0.f ? w->rope_sin : nullptr;
       g.epi.rope_positions = w->rope_positions;
+      fold_in(g.epi);
       const double b = (static_cast<double>(nqkv) * D + static_cast<double>(rows) * (D + nqkv)) * es;
       if ((st = run_gemm(cx, g, m_qkv, m_xn, p_qkv, b, 2.0 * rows * nqkv * static_cast<double>(D))) != DFLASH_OK)
         return st;
@@ -564,6 +613,7 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
       a.layer = l;
       a.n_layers = Lyr;
       a.ctx_len = ctx_len; a.out = ao;
+      a.out_lo_off = ao_lo;
       a.dev_status = dev_status;
       a.B = B; a.R = R; a.n_q_heads = c->n_q_heads; a.n_kv_heads = c->n_kv_heads;
       a.head_dim = c->head_dim; a.ncap = c->ctx_capacity; a.max_batch = c->max_batch;
@@ -575,42 +625,47 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
       cx.tr.after();
       if (st != DFLASH_OK) return st;
     }
-    // output projection + residual
+    // output projection + residual; emits g_ffn (.) h and sums of squares
     {
       GemmArgs g{};
       g.k = HD; g.m_rows = D; g.n_rows = rows; g.swap = 1; g.a_weights = 1; g.a_z0 = l;
+      g.b_pack = pack_of(s_ao, rows); g.b_box_rows = box_of(p_o, rows);
       g.dev_status = dev_status;
       g.epi = base_epi(c);
       g.epi.op = EPI_ADD_F32; g.epi.out = h; g.epi.ld = D; g.epi.n_tok = rows; g.epi.n_feat = D;
+      fold_out(g.epi, xn, gain_of(w->g_ffn, l), 0);
       const double b = static_cast<double>(D) * HD * es + static_cast<double>(rows) * HD * es + 2.0 * row_bytes;
       if ((st = run_gemm(cx, g, m_o, m_ao, p_o, b, 2.0 * rows * D * static_cast<double>(HD))) != DFLASH_OK)
         return st;
     }
-    // FFN input norm
-    cx.tr.before(DFLASH_K_NORM, row_bytes + static_cast<double>(rows) * D * es, 0);
-    st = fail(launch_rmsnorm(h, static_cast<const uint8_t*>(w->g_ffn) + gain_off, xn, rows, D,
-                             c->rms_eps, bf16, 0, c->gamma, R, cx.s, cx.pdl));
-    cx.tr.after();
-    if (st != DFLASH_OK) return st;
-    // gate|up + SwiGLU
+    // gate|up of RMSNorm(h) + SwiGLU
     {
       GemmArgs g{};
       g.k = D; g.m_rows = 2 * F; g.n_rows = rows; g.swap = 1; g.a_weights = 1; g.a_z0 = l;
       g.a_gateup = F;
+      g.b_pack = pack_of(s_xn, rows); g.b_box_rows = box_of(p_gu, rows);
       g.dev_status = dev_status;
       g.epi = base_epi(c);
       g.epi.op = EPI_SWIGLU; g.epi.out = act; g.epi.ld = F; g.epi.n_tok = rows; g.epi.n_feat = F;
+      g.epi.lo_off = act_lo;
+      fold_in(g.epi);
       const double b = (2.0 * F * D + static_cast<double>(rows) * (D + F)) * es;
       if ((st = run_gemm(cx, g, m_gu, m_xn_gu, p_gu, b, 4.0 * rows * F * static_cast<double>(D))) != DFLASH_OK)
         return st;
     }
-    // down + residual
+    // down + residual; emits the next layer's g_attn (.) h, or for the last
+    // layer the final norm's g_final (.) h of the mask rows
     {
       GemmArgs g{};
       g.k = F; g.m_rows = D; g.n_rows = rows; g.swap = 1; g.a_weights = 1; g.a_z0 = l;
+      g.b_pack = pack_of(s_act, rows); g.b_box_rows = box_of(p_dn, rows);
       g.dev_status = dev_status;
       g.epi = base_epi(c);
       g.epi.op = EPI_ADD_F32; g.epi.out = h; g.epi.ld = D; g.epi.n_tok = rows; g.epi.n_feat = D;
+      if (l + 1 < Lyr)
+        fold_out(g.epi, xn, gain_of(w->g_attn, l + 1), 0);
+      else
+        fold_out(g.epi, z, w->g_final, 1);
       const double b = static_cast<double>(D) * F * es + static_cast<double>(rows) * F * es + 2.0 * row_bytes;
       if ((st = run_gemm(cx, g, m_dn, m_act, p_dn, b, 2.0 * rows * D * static_cast<double>(F))) != DFLASH_OK)
         return st;
@@ -620,18 +675,16 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
                         static_cast<size_t>(rows) * D, cx.s, cx.pdl) != cudaSuccess)
       return DFLASH_ERR_CUDA;
   }
-  // final norm of the mask rows, LM head with fused argmax
-  cx.tr.before(DFLASH_K_NORM, static_cast<double>(nmask) * D * (4 + es), 0);
-  st = fail(launch_rmsnorm(h, w->g_final, z, nmask, D, c->rms_eps, bf16, 1, c->gamma, R, cx.s, cx.pdl));
-  cx.tr.after();
-  if (st != DFLASH_OK) return st;
+  // LM head of RMSNorm(h[mask rows]) with fused argmax
   {
     GemmArgs g{};
     g.k = D; g.m_rows = V; g.n_rows = nmask; g.swap = 1; g.a_weights = 1;
+    g.b_pack = pack_of(s_z, nmask); g.b_box_rows = box_of(p_lm, nmask);
     g.dev_status = dev_status;
     g.epi = base_epi(c);
     g.epi.op = EPI_ARGMAX; g.epi.out = logits_opt; g.epi.ld = V; g.epi.n_tok = nmask; g.epi.n_feat = V;
     g.epi.keys = keys;
+    fold_in(g.epi);
     const double b = (static_cast<double>(V) * D + static_cast<double>(nmask) * D) * es;
     if ((st = run_gemm(cx, g, m_lm, m_z, p_lm, b, 2.0 * nmask * V * static_cast<double>(D))) != DFLASH_OK)
       return st;

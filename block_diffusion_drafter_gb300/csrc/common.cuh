@@ -246,6 +246,14 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 }
 
 // ----------------------------------------------------------------- misc
+// Split of an fp32 value into two bf16 parts, hi = bf16(x) and lo = bf16(x - hi);
+// hi + lo carries ~16 mantissa bits. Projections multiply both parts into one
+// fp32 accumulator, so their activation operand is not limited to bf16 precision.
+__device__ __forceinline__ void store_hilo(__nv_bfloat16* p, size_t idx, size_t lo_off, float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  p[idx] = hi;
+  if (lo_off) p[idx + lo_off] = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
 template <>

@@ -28,7 +28,7 @@ namespace {
 
 constexpr int kSLD = 129;  // staging row stride (floats): conflict-free both ways
 // barriers + token table, plus slack to align the tile ring to 1024 bytes
-constexpr size_t kSmemHeaderBytes = 4096;
+constexpr size_t kSmemHeaderBytes = 3072;
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
@@ -48,25 +48,60 @@ __device__ __forceinline__ void store_out(void* out, int bf16, size_t idx, float
 constexpr int kEpiBatch = 8;
 
 struct TokInfo {
-  int pos[kBM];   // cache position of the tile's token x, -1 = skip
-  int seq[kBM];   // sequence of token x
+  int pos[kBM];     // cache position of the tile's token x, -1 = skip
+  int seq[kBM];     // sequence of token x
+  float rstd[kBM];  // folded RMSNorm scale of token x (1 when not folded)
 };
 
+__device__ __forceinline__ float gain_at(const void* g, int bf16, int i) {
+  return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(g)[i])
+              : reinterpret_cast<const float*>(g)[i];
+}
+
+// Folded RMSNorm scale 1 / sqrt(mean(h^2) + eps) of tokens tok0 .. tok0+n-1
+// into out[0 .. n), from their per-128-feature partial sums of squares: one
+// warp per token, lane k adds slots k, k+32, ... (fixed order), then a
+// shuffle tree. Tokens past n_tok get 1. Runs on the 128 epilogue threads.
+__device__ __forceinline__ void folded_rstd(const Epi& e, float* out, int tok0, int n, int etid) {
+  const int w = etid >> 5, lane = etid & 31;
+  for (int t = w; t < n; t += 4) {
+    const int tok = tok0 + t;
+    float ss = 0.f;
+    if (tok < e.n_tok)
+      for (int k = lane; k < e.n_ss; k += 32) ss += e.ss_in[static_cast<size_t>(tok) * e.n_ss + k];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (lane == 0) out[t] = tok < e.n_tok ? 1.0f / sqrtf(ss / static_cast<float>(e.d_model) + e.eps) : 1.f;
+  }
+}
+
+// Whether the kernel computes the folded-norm scales of the whole tile (one
+// per B row) while the main loop runs, instead of per chunk in the epilogue.
+__device__ __forceinline__ bool rstd_per_tile(const GemmArgs& g) {
+  return g.epi.ss_in != nullptr && g.swap != 0 && g.bn <= kBM;
+}
+
+template <int kOp>
 __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, int col0, int cols,
                                int m_tile, int n_tile, int etid) {
   const Epi& e = g.epi;
   const int total = cols * kBM;
   const bool tok_cols = g.swap != 0;  // tokens along B rows (columns of S)
-  if (e.op == EPI_QKV || e.op == EPI_KV) {
+  // rstd[x]: folded-norm scale of the chunk's token x
+  const bool pre = rstd_per_tile(g);
+  const float* rstd = ti->rstd + (pre ? col0 : 0);
+  if (e.ss_in != nullptr && !pre)
+    folded_rstd(e, ti->rstd, tok_cols ? n_tile * g.bn + col0 : m_tile * kBM, tok_cols ? cols : kBM, etid);
+  if (kOp == EPI_QKV || kOp == EPI_KV || (e.ss_in != nullptr && !pre)) {
     const int nloc = tok_cols ? cols : kBM;
     for (int x = etid; x < nloc; x += 128) {
       const int tok = tok_cols ? n_tile * g.bn + col0 + x : m_tile * kBM + x;
       int pos = -1, seq = 0;
-      if (tok < e.n_tok) {
+      if ((kOp == EPI_QKV || kOp == EPI_KV) && tok < e.n_tok) {
         seq = tok / e.rows_per_seq;
         const int t = tok - seq * e.rows_per_seq;
         const int base = e.ctx_len[seq];
-        if (e.op == EPI_QKV) {
+        if (kOp == EPI_QKV) {
           pos = base + t;
           if (pos >= e.ncap) { report(g.dev_status, DFLASH_ERR_CAPACITY); pos = -1; }
         } else {
@@ -79,10 +114,15 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
     }
     named_bar(1, 128);
   }
-  switch (e.op) {
+  switch (kOp) {
     case EPI_STORE:
     case EPI_ADD_F32:
     case EPI_FUSE: {
+      // producer of a folded norm (swap orientation): this thread's feature is
+      // m_tile * 128 + etid for every element it touches
+      const float gx = kOp == EPI_ADD_F32 && e.xg_out != nullptr && m_tile * kBM + etid < e.n_feat
+                           ? gain_at(e.xg_gain, e.xg_bf16, m_tile * kBM + etid)
+                           : 0.f;
       for (int base = etid; base < total; base += 128 * kEpiBatch) {
         float v[kEpiBatch], r[kEpiBatch];
         size_t o[kEpiBatch];
@@ -96,22 +136,70 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           const int tok = g.swap ? n_tile * g.bn + col0 + b : m_tile * kBM + a;
           ok[u] = idx < total && tok < e.n_tok && feat < e.n_feat;
           v[u] = ok[u] ? S[b * kSLD + a] : 0.f;
+          if (e.ss_in != nullptr && ok[u]) v[u] *= rstd[tok_cols ? b : a];
           o[u] = static_cast<size_t>(tok) * e.ld + feat;
         }
-        if (e.op == EPI_ADD_F32) {
+        if (kOp == EPI_ADD_F32) {
 #pragma unroll
           for (int u = 0; u < kEpiBatch; ++u)
             r[u] = ok[u] ? reinterpret_cast<const float*>(e.out)[o[u]] : 0.f;
 #pragma unroll
-          for (int u = 0; u < kEpiBatch; ++u)
-            if (ok[u]) reinterpret_cast<float*>(e.out)[o[u]] = r[u] + v[u];
+          for (int u = 0; u < kEpiBatch; ++u) {
+            if (!ok[u]) continue;
+            const float hn = r[u] + v[u];
+            reinterpret_cast<float*>(e.out)[o[u]] = hn;
+            if (e.xg_out != nullptr) {
+              // folded RMSNorm of the next projection: g (.) h_new and h_new^2
+              const int idx = base + u * 128;
+              const int a = idx & 127, b = idx >> 7;   // swap orientation
+              const int tok = n_tile * g.bn + col0 + b;
+              const int feat = m_tile * kBM + a;
+              int row = tok;
+              if (e.xg_mask_rows) {
+                const int i = tok % e.rows_per_seq;
+                row = i == 0 ? -1 : (tok / e.rows_per_seq) * e.gamma + i - 1;
+              }
+              if (row >= 0) {
+                const size_t xi = static_cast<size_t>(row) * e.d_model + feat;
+                const float xv = gx * hn;
+                if (e.xg_bf16)
+                  store_hilo(reinterpret_cast<__nv_bfloat16*>(e.xg_out), xi, e.lo_off, xv);
+                else
+                  reinterpret_cast<float*>(e.xg_out)[xi] = xv;
+              }
+              const_cast<float*>(S)[b * kSLD + a] = hn * hn;
+            }
+          }
         } else {
 #pragma unroll
           for (int u = 0; u < kEpiBatch; ++u)
             if (ok[u]) store_out(e.out, e.out_bf16, o[u], v[u]);
         }
       }
-      if (e.op == EPI_FUSE) {
+      if (kOp == EPI_ADD_F32 && e.xg_out != nullptr) {
+        // per token: sum of h_new^2 over the tile's 128 features (fixed order:
+        // four strided partials per lane, then a shuffle tree)
+        named_bar(1, 128);
+        const int w = etid >> 5, lane = etid & 31;
+        for (int b = w; b < cols; b += 4) {
+          const int tok = n_tile * g.bn + col0 + b;
+          float sacc = 0.f;
+          for (int i = 0; i < 4; ++i) {
+            const int a = lane + 32 * i;
+            if (tok < e.n_tok && m_tile * kBM + a < e.n_feat) sacc += S[b * kSLD + a];
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, off);
+          int row = tok;
+          if (e.xg_mask_rows) {
+            const int i = tok % e.rows_per_seq;
+            row = i == 0 ? -1 : (tok / e.rows_per_seq) * e.gamma + i - 1;
+          }
+          if (lane == 0 && tok < e.n_tok && row >= 0)
+            e.ss_out[static_cast<size_t>(row) * e.n_ss + m_tile] = sacc;
+        }
+      }
+      if (kOp == EPI_FUSE) {
         // Per token: sum of squares over this chunk's 128 features, summed
         // sequentially (fixed order), one slot per 128-feature group.
         if (g.swap) {
@@ -141,8 +229,13 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
         const int feat = m_tile * 64 + a;
         const int tok = n_tile * g.bn + col0 + b;
         if (tok >= e.n_tok || feat >= e.n_feat) continue;
-        const float gate = S[b * kSLD + a], up = S[b * kSLD + a + 64];
-        store_out(e.out, e.out_bf16, static_cast<size_t>(tok) * e.ld + feat, silu_f(gate) * up);
+        const float rs = e.ss_in != nullptr ? rstd[b] : 1.f;
+        const float gate = S[b * kSLD + a] * rs, up = S[b * kSLD + a + 64] * rs;
+        const size_t oi = static_cast<size_t>(tok) * e.ld + feat;
+        if (e.out_bf16)
+          store_hilo(reinterpret_cast<__nv_bfloat16*>(e.out), oi, e.lo_off, silu_f(gate) * up);
+        else
+          reinterpret_cast<float*>(e.out)[oi] = silu_f(gate) * up;
       }
       break;
     }
@@ -154,7 +247,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
         float y[kEpiBatch], cs[kEpiBatch], sn[kEpiBatch];
         size_t o[kEpiBatch];
         int kind[kEpiBatch];  // 0 skip, 1 q, 2 k, 3 v
-        int dd[kEpiBatch], pp[kEpiBatch];
+        int dd[kEpiBatch], pp[kEpiBatch], xx[kEpiBatch];
 #pragma unroll
         for (int u = 0; u < kEpiBatch; ++u) {
           const int idx = base + u * 128;
@@ -166,12 +259,13 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           kind[u] = 0;
           dd[u] = 0;
           pp[u] = 0;
+          xx[u] = x;
           o[u] = 0;
           y[u] = 0.f;
           if (idx < total && gf < e.n_feat) {
             const int pos = ti->pos[x], seq = ti->seq[x];
             int f = gf, layer = e.layer;
-            if (e.op == EPI_KV) {
+            if (kOp == EPI_KV) {
               layer = gf / e.feat_per_layer;
               f = gf - layer * e.feat_per_layer + nq;   // position within the [Q; K; V] rows
             }
@@ -217,6 +311,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           float val = y[u];
           if (kind[u] != 3 && e.rope_cos != nullptr)
             val = dd[u] < half ? y[u] * c[u] - cs[u] * sv[u] : y[u] * c[u] + cs[u] * sv[u];
+          if (e.ss_in != nullptr) val *= rstd[xx[u]];
           void* dst = kind[u] == 1 ? e.out : (kind[u] == 2 ? e.k_cache : e.v_cache);
           store_out(dst, e.out_bf16, o[u], val);
         }
@@ -235,7 +330,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           const int a = lane + 32 * i;
           const int feat = m_tile * kBM + a;
           if (feat < e.n_feat) {
-            const float v = S[b * kSLD + a];
+            const float v = S[b * kSLD + a] * (e.ss_in != nullptr ? rstd[b] : 1.f);
             const unsigned long long key = argmax_key(v, static_cast<uint32_t>(feat));
             best = key > best ? key : best;
             if (e.out != nullptr && tok < e.n_tok)
@@ -272,7 +367,11 @@ struct SmemHeader {
   TokInfo tok;
 };
 
-template <bool kTF32>
+static_assert(sizeof(SmemHeader) + 1023 <= kSmemHeaderBytes, "shared-memory header allowance");
+
+// One instantiation per (operand type, split activations, epilogue op), so
+// that each launch runs only the code of its own case.
+template <bool kTF32, bool kSplit, int kOp>
 __global__ void __launch_bounds__(kGemmThreads)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap a_map,
                    const __grid_constant__ CUtensorMap b_map, const GemmArgs g, int stages) {
@@ -289,9 +388,14 @@ __global__ void __launch_bounds__(kGemmThreads)
   const int kt0 = split * g.kt_per_split;
   const int nkt = min(g.kt_per_split, KT - kt0);
   const uint32_t a_bytes = kBM * 128u;
-  const uint32_t b_bytes = static_cast<uint32_t>(g.bn) * 128u;
-  const uint32_t stage_bytes = a_bytes + b_bytes;
+  constexpr bool b_split = kSplit;  // hi and lo rows packed in the tile (g.b_pack each)
+  const uint32_t b_tile = static_cast<uint32_t>(g.bn) * 128u;
   const int sub_rows = g.bn / g.n_sub;
+  const int box_rows = g.b_box_rows > 0 ? g.b_box_rows : sub_rows;    // rows each B box brings
+  // ring stride in shared memory (whole tiles, 1024-byte aligned) and the
+  // bytes the TMA loads of one stage actually bring
+  const uint32_t stage_stride = a_bytes + b_tile;
+  const uint32_t stage_tx = a_bytes + static_cast<uint32_t>(g.n_sub * box_rows) * 128u;
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(g.bn)) tmem_cols <<= 1;
 
@@ -332,7 +436,7 @@ __global__ void __launch_bounds__(kGemmThreads)
       const int b_y = g.b_row0 + (n_tile % g.b_tiles_per_z) * g.bn;
       const int b_z = g.b_z0 + n_tile / g.b_tiles_per_z;
       auto load_a = [&](int s, int kt) {
-        const uint32_t dst = tiles_s + s * stage_bytes;
+        const uint32_t dst = tiles_s + s * stage_stride;
         const uint32_t bar = smem_u32(&hdr->full[s]);
         if (g.a_gateup > 0) {
           tma_load_3d(dst, &a_map, bar, kt * kBK, a_y, a_z, pol_a);
@@ -342,11 +446,12 @@ __global__ void __launch_bounds__(kGemmThreads)
         }
       };
       auto load_b = [&](int s, int kt) {
-        const uint32_t dst = tiles_s + s * stage_bytes + a_bytes;
+        const uint32_t dst = tiles_s + s * stage_stride + a_bytes;
         const uint32_t bar = smem_u32(&hdr->full[s]);
-        for (int sub = 0; sub < g.n_sub; ++sub)
+        for (int sub = 0; sub < g.n_sub; ++sub) {
           tma_load_3d(dst + sub * sub_rows * 128, &b_map, bar, kt * kBK, b_y + sub * sub_rows, b_z,
                       pol_b);
+        }
       };
       // Weights do not depend on the previous kernel: start streaming them
       // before waiting for it (programmatic dependent launch).
@@ -354,7 +459,7 @@ __global__ void __launch_bounds__(kGemmThreads)
       if (g.a_weights) {
         n_pre = min(stages, nkt);
         for (int it = 0; it < n_pre; ++it) {
-          mbar_expect_tx(smem_u32(&hdr->full[it]), stage_bytes);
+          mbar_expect_tx(smem_u32(&hdr->full[it]), stage_tx);
           load_a(it, kt0 + it);
         }
       }
@@ -368,7 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads)
           break;
         }
         if (*reinterpret_cast<volatile int*>(&hdr->abort_flag)) break;
-        mbar_expect_tx(smem_u32(&hdr->full[s]), stage_bytes);
+        mbar_expect_tx(smem_u32(&hdr->full[s]), stage_tx);
         load_a(s, kt0 + it);
         load_b(s, kt0 + it);
       }
@@ -386,7 +491,7 @@ __global__ void __launch_bounds__(kGemmThreads)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = tiles_s + s * stage_bytes;
+        const uint32_t a_addr = tiles_s + s * stage_stride;
         const uint32_t b_addr = a_addr + a_bytes;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of k per 128-byte row
@@ -394,10 +499,11 @@ __global__ void __launch_bounds__(kGemmThreads)
           for (int sub = 0; sub < g.n_sub; ++sub) {
             const uint64_t bdesc = sw128_desc(b_addr + sub * sub_rows * 128 + k * 32);
             const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-            if (kTF32)
+            if (kTF32) {
               tc_mma_tf32(tmem + sub * sub_rows, adesc, bdesc, idesc, acc);
-            else
+            } else {
               tc_mma_f16(tmem + sub * sub_rows, adesc, bdesc, idesc, acc);
+            }
           }
         }
         tc_commit(smem_u32(&hdr->empty[s]));
@@ -413,6 +519,8 @@ __global__ void __launch_bounds__(kGemmThreads)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* S = reinterpret_cast<float*>(tiles); // staging reuses the drained pipeline
     pdl_wait();
+    // folded-norm scales of the tile's tokens, off the critical path
+    if (rstd_per_tile(g)) folded_rstd(g.epi, hdr->tok.rstd, n_tile * g.bn, g.bn, etid);
     if (!mbar_wait(smem_u32(&hdr->accum), 0)) {
       report(g.dev_status, DFLASH_ERR_TIMEOUT);
       atomicExch(&hdr->abort_flag, 1);
@@ -436,8 +544,12 @@ __global__ void __launch_bounds__(kGemmThreads)
 #pragma unroll
             for (int i = 0; i < 16; ++i) S[(j + i) * kSLD + row] = v[i];
           }
+          // packed split operands: token j = hi product + lo product (this
+          // thread's own row of the staging tile, so no barrier is needed)
+          if (b_split)
+            for (int j = 0; j < g.b_pack; ++j) S[j * kSLD + row] += S[(g.b_pack + j) * kSLD + row];
           named_bar(1, 128);
-          apply_epilogue(g, S, &hdr->tok, c * kBM, cols, m_tile, n_tile, etid);
+          apply_epilogue<kOp>(g, S, &hdr->tok, c * kBM, cols, m_tile, n_tile, etid);
           named_bar(1, 128);
         }
       } else {
@@ -451,6 +563,8 @@ __global__ void __launch_bounds__(kGemmThreads)
 #pragma unroll
           for (int i = 0; i < 16; ++i) P[(j + i) * kBM + row] = v[i];
         }
+        if (b_split)
+          for (int j = 0; j < g.b_pack; ++j) P[j * kBM + row] += P[(g.b_pack + j) * kBM + row];
       }
     }
     tc_fence_before();
@@ -491,7 +605,7 @@ __global__ void __launch_bounds__(kGemmThreads)
           }
         }
         named_bar(1, 128);
-        if (ok) apply_epilogue(g, S, &hdr->tok, cb, cols, m_tile, n_tile, etid);
+        if (ok) apply_epilogue<kOp>(g, S, &hdr->tok, cb, cols, m_tile, n_tile, etid);
         named_bar(1, 128);
       }
     }
@@ -542,11 +656,14 @@ bool make_operand_map(CUtensorMap* map, const void* base, int elem_bytes, uint64
 }
 
 GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
-                   int bn_cap) {
+                   int bn_cap, bool b_split) {
   GemmPlan p{};
   const int bk = 128 / elem_bytes;
   const int KT = k / bk;
-  const int n16 = (n_rows + 15) / 16 * 16;
+  // split activations: one tile holding the hi and the lo rows of every
+  // token (two rows per token), for up to 128 tokens
+  b_split = b_split && 2 * n_rows <= (bn_cap < 256 ? bn_cap : 256);
+  const int n16 = ((b_split ? 2 * n_rows : n_rows) + 15) / 16 * 16;
   const int cap1 = bn_cap < 256 ? bn_cap : 256;
   if (n16 <= cap1) {
     p.bn = n16; p.n_sub = 1; p.n_tiles = 1;
@@ -559,6 +676,7 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   // Weight streaming wants many resident CTAs more than deep pipelines: a
   // short ring (3 stages) leaves room for 3 CTAs per SM on the skinny
   // shapes, whose prologue/epilogue then overlap other CTAs' streaming.
+  p.b_split = b_split ? 1 : 0;
   const size_t stage = 16384 + static_cast<size_t>(p.bn) * 128;
   const size_t staging = static_cast<size_t>(p.bn < kBM ? p.bn : kBM) * 129 * 4;
   int stages = p.bn <= 128 ? 3 : static_cast<int>((222 * 1024 - kSmemHeaderBytes) / stage);
@@ -597,18 +715,41 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   }
   p.kt_per_split = (KT + splits - 1) / splits;
   p.splits = (KT + p.kt_per_split - 1) / p.kt_per_split;
+  // without split-K the epilogue drains 128 columns at a time, and a packed
+  // tile must pair each token's hi and lo columns inside one drain
+  if (b_split && p.splits == 1 && p.bn > kBM)
+    return plan_gemm(m_tiles, n_rows, k, elem_bytes, num_sms, allow_split, bn_cap, false);
   p.partial_bytes = 0;
   return p;
 }
 
+using GemmKernel = void (*)(const CUtensorMap, const CUtensorMap, const GemmArgs, int);
+
+template <bool kTF32, bool kSplit, int... kOps>
+struct GemmKernelRow {
+  static constexpr GemmKernel fns[sizeof...(kOps)] = {&gemm_tc_kernel<kTF32, kSplit, kOps>...};
+};
+constexpr int kNumEpiOps = 7;
+static_assert(EPI_FUSE == kNumEpiOps - 1, "one kernel per epilogue op");
+// [tf32 | bf16 | bf16 with split activations][epilogue op]
+const GemmKernel* const kGemmKernels[3] = {
+    GemmKernelRow<true, false, 0, 1, 2, 3, 4, 5, 6>::fns,
+    GemmKernelRow<false, false, 0, 1, 2, 3, 4, 5, 6>::fns,
+    GemmKernelRow<false, true, 0, 1, 2, 3, 4, 5, 6>::fns,
+};
+
 cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const GemmArgs& args,
                         const GemmPlan& plan, cudaStream_t stream, bool pdl) {
-  void (*kern)(const CUtensorMap, const CUtensorMap, const GemmArgs, int) =
-      args.tf32 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
-  static bool configured[2][64] = {};
+  const bool split = args.b_pack > 0;
+  if (args.tf32 && split) return cudaErrorInvalidValue;  // split operands are bf16 only
+  if (split != (plan.b_split != 0)) return cudaErrorInvalidValue;  // plan sized the other ring
+  if (args.epi.op < 0 || args.epi.op >= kNumEpiOps) return cudaErrorInvalidValue;
+  const int variant = args.tf32 ? 0 : (split ? 2 : 1);
+  const GemmKernel kern = kGemmKernels[variant][args.epi.op];
+  static bool configured[3][kNumEpiOps][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  bool& done = configured[args.tf32 ? 1 : 0][dev & 63];
+  bool& done = configured[variant][args.epi.op][dev & 63];
   if (!done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;

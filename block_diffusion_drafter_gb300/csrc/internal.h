@@ -49,6 +49,24 @@ struct Epi {
   // EPI_FUSE
   float* row_ss;      // [n_tok, n_ss] partial sums of squares
   int n_ss;
+  // RMSNorm folded into the projections. Consumer side: when ss_in is set,
+  // the accumulator of token t is scaled by rstd[t] = 1/sqrt(sum(ss_in[t]) / d_model + eps)
+  // (its B operand is g (.) h, so the product equals W RMSNorm(h)).
+  // Producer side (EPI_ADD_F32): when xg_out is set, also writes
+  // xg_out[row] = g (.) h_new (cfg dtype) and ss_out[row][m_tile] = sum over
+  // the tile's 128 features of h_new^2; xg_mask_rows maps token b*R + i to
+  // row b*gamma + i - 1 and skips the anchor rows (the final norm's rows).
+  const float* ss_in;
+  void* xg_out;
+  const void* xg_gain;
+  float* ss_out;
+  int xg_mask_rows;
+  int xg_bf16;        // element type of xg_out and xg_gain
+  size_t lo_off;      // > 0: bf16 outputs feeding a projection (xg_out, or out of
+                      // EPI_SWIGLU) also get lo = bf16(x - hi) at + lo_off elements
+  int gamma;
+  int d_model;
+  float eps;
 };
 
 struct GemmArgs {
@@ -64,6 +82,11 @@ struct GemmArgs {
   int a_row0, a_z0, a_tiles_per_z;
   int b_row0, b_z0, b_tiles_per_z;
   int a_gateup;       // > 0: A tile = 64 rows at a_row0 + 64*m and 64 rows at a_row0 + a_gateup + 64*m
+  int b_pack;         // > 0: split activations packed in one B tile: rows [0, b_pack) hold
+                      //      hi = bf16(x) and rows [b_pack, 2 b_pack) lo = bf16(x - hi) of
+                      //      the same tokens; accumulator column b_pack + j is added to column j
+  int b_box_rows;     // rows per B box of the tensor map (0: bn / n_sub); rows of a tile
+                      // past the box are never loaded and feed only unused accumulator columns
   int swap;           // 1: A rows are output features and B rows tokens; 0: the reverse
   int a_weights;      // 1: A is a weight (independent of earlier kernels): prefetch before PDL wait
   int tf32;           // 1: fp32 operands through kind::tf32
@@ -73,6 +96,7 @@ struct GemmArgs {
 
 struct GemmPlan {
   int bn, n_sub, splits, kt_per_split, m_tiles, n_tiles, stages;
+  int b_split;        // B tile packs hi and lo rows (bn covers 2 n_rows)
   size_t smem_bytes;
   size_t partial_bytes;
 };
@@ -80,7 +104,7 @@ struct GemmPlan {
 // Chooses tile shape, split count and pipeline depth for m_tiles A tiles
 // against n_rows B rows over k (elements of elem_bytes each).
 GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
-                   int bn_cap = kMaxBN);
+                   int bn_cap = kMaxBN, bool b_split = false);
 
 // Builds a 3-D tensor map over a [z][rows][k] row-major operand with a box of
 // (64 or 32 elements of k) x box_rows x 1 and 128-byte swizzle.
@@ -98,6 +122,7 @@ struct AttnArgs {
   int layer, n_layers;
   const int* ctx_len;     // [B]
   void* out;              // [B*R, Hq*Dh]
+  size_t out_lo_off;      // > 0: bf16 lo = bf16(o - hi) at out + out_lo_off elements
   int* dev_status;
   int B, R, n_q_heads, n_kv_heads, head_dim, ncap, max_batch;
   int splits, chunk;      // keys per split (multiple of 64); last split takes the rest;
@@ -111,13 +136,13 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl);
 
 // Small row kernels.
+// h[b*R + i] = embed[id] (id = anchor[b] for i == 0, else mask_id), fp32; also
+// xg = gain (.) h in cfg dtype and ss[row][c] = sum of h^2 over features
+// 128c..128c+127 (the first layer's folded RMSNorm); zeroes keys[0..n_keys).
 cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
-                         int bf16, float* h, unsigned long long* keys, int n_keys, int* dev_status,
-                         cudaStream_t s, bool pdl);
-// out row r = RMSNorm(x row src(r)); src(r) = r when mask_rows == 0, else
-// (r / gamma) * R + 1 + r % gamma (the mask rows of each block).
-cudaError_t launch_rmsnorm(const float* x, const void* gain, void* out, int rows, int D, float eps,
-                           int bf16, int mask_rows, int gamma, int R, cudaStream_t s, bool pdl);
+                         int bf16, float* h, const void* gain, void* xg, size_t xg_lo_off, float* ss,
+                         unsigned long long* keys, int n_keys, int* dev_status, cudaStream_t s,
+                         bool pdl);
 // h[t] = gain * u[t] / sqrt(sum(row_ss[t]) / D + eps), u fp32, h in cfg dtype.
 cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
                              int T, int D, float eps, int bf16, cudaStream_t s, bool pdl);

@@ -23,25 +23,6 @@ cudaError_t launch_ex(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
-// Block-wide fp32 sum with a fixed reduction tree (256 threads).
-__device__ __forceinline__ float block_sum256(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) red[w] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x < 32) {
-    t = lane < 8 ? red[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) red[8] = t;
-  }
-  __syncthreads();
-  return red[8];
-}
-
 // Loads of one row are issued up front (float4, up to kRowVec per thread) so a
 // row costs one memory latency rather than one per strided iteration.
 constexpr int kRowVec = 8;  // rows up to 256 threads x 8 float4 = 8192 floats
@@ -71,9 +52,21 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* src)
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// x - bf16(x) per component (the lo part of a split bf16 value); 0 for fp32.
+template <typename T>
+__device__ __forceinline__ float4 sub_hi4(float4 x);
+template <>
+__device__ __forceinline__ float4 sub_hi4<float>(float4) { return make_float4(0.f, 0.f, 0.f, 0.f); }
+template <>
+__device__ __forceinline__ float4 sub_hi4<__nv_bfloat16>(float4 x) {
+  auto r = [](float v) { return v - __bfloat162float(__float2bfloat16_rn(v)); };
+  return make_float4(r(x.x), r(x.y), r(x.z), r(x.w));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* anchor, int mask_id,
-                                                    int R, int D, int V, float* h,
+                                                    int R, int D, int V, float* h, const T* gain,
+                                                    T* xg, size_t xg_lo_off, float* ss,
                                                     unsigned long long* keys, int n_keys,
                                                     int* dev_status) {
   pdl_launch_dependents();
@@ -86,53 +79,33 @@ __global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* a
   }
   const T* src = embed + static_cast<size_t>(id) * D;
   float* dst = h + static_cast<size_t>(r) * D;
+  T* xr = xg + static_cast<size_t>(r) * D;
   const int n4 = D / 4;
   float4 v[kRowVec];
 #pragma unroll
-  for (int i = 0; i < kRowVec; ++i) {
-    const int q = threadIdx.x + i * blockDim.x;
-    if (q < n4) v[i] = load4<T>(src + 4 * q);
+  for (int i4 = 0; i4 < kRowVec; ++i4) {
+    const int q = threadIdx.x + i4 * blockDim.x;
+    if (q < n4) v[i4] = load4<T>(src + 4 * q);
   }
 #pragma unroll
-  for (int i = 0; i < kRowVec; ++i) {
-    const int q = threadIdx.x + i * blockDim.x;
-    if (q < n4) reinterpret_cast<float4*>(dst)[q] = v[i];
+  for (int i4 = 0; i4 < kRowVec; ++i4) {
+    const int q = threadIdx.x + i4 * blockDim.x;
+    if (q < n4) {
+      reinterpret_cast<float4*>(dst)[q] = v[i4];
+      const float4 g = load4<T>(gain + 4 * q);
+      const float4 x = make_float4(g.x * v[i4].x, g.y * v[i4].y, g.z * v[i4].z, g.w * v[i4].w);
+      store4<T>(xr + 4 * q, x);
+      if (xg_lo_off) store4<T>(xr + xg_lo_off + 4 * q, sub_hi4<T>(x));
+    }
+    // one warp holds one 128-feature slot (32 lanes x 4 features): sum of h^2
+    // per slot in a fixed shuffle order
+    float sq = q < n4 ? v[i4].x * v[i4].x + v[i4].y * v[i4].y + v[i4].z * v[i4].z + v[i4].w * v[i4].w : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    if ((threadIdx.x & 31) == 0 && q < n4) ss[static_cast<size_t>(r) * (D / 128) + q / 32] = sq;
   }
   if (blockIdx.x == 0)
     for (int k = threadIdx.x; k < n_keys; k += blockDim.x) keys[k] = 0ull;
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, const T* gain, T* out, int D,
-                                                      float eps, int mask_rows, int gamma, int R) {
-  __shared__ float red[9];
-  pdl_launch_dependents();
-  pdl_wait();
-  const int r = blockIdx.x;
-  const int src = mask_rows ? (r / gamma) * R + 1 + r % gamma : r;
-  const float* xr = x + static_cast<size_t>(src) * D;
-  const int n4 = D / 4;
-  float4 v[kRowVec];
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < kRowVec; ++i) {
-    const int q = threadIdx.x + i * blockDim.x;
-    v[i] = q < n4 ? reinterpret_cast<const float4*>(xr)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll
-  for (int i = 0; i < kRowVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-  ss = block_sum256(ss, red);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
-  T* o = out + static_cast<size_t>(r) * D;
-#pragma unroll
-  for (int i = 0; i < kRowVec; ++i) {
-    const int q = threadIdx.x + i * blockDim.x;
-    if (q < n4) {
-      const float4 g = load4<T>(gain + 4 * q);
-      store4<T>(o + 4 * q, make_float4(g.x * v[i].x * inv, g.y * v[i].y * inv, g.z * v[i].z * inv,
-                                       g.w * v[i].w * inv));
-    }
-  }
 }
 
 template <typename T>
@@ -268,26 +241,18 @@ __global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int3
 }  // namespace
 
 cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
-                         int bf16, float* h, unsigned long long* keys, int n_keys, int* dev_status,
-                         cudaStream_t s, bool pdl) {
+                         int bf16, float* h, const void* gain, void* xg, size_t xg_lo_off, float* ss,
+                         unsigned long long* keys, int n_keys, int* dev_status, cudaStream_t s,
+                         bool pdl) {
   if (bf16)
     return launch_ex(embed_kernel<__nv_bfloat16>, dim3(B * R), dim3(256), 0, s, pdl,
-                     reinterpret_cast<const __nv_bfloat16*>(embed), anchor, mask_id, R, D, V, h, keys,
-                     n_keys, dev_status);
+                     reinterpret_cast<const __nv_bfloat16*>(embed), anchor, mask_id, R, D, V, h,
+                     reinterpret_cast<const __nv_bfloat16*>(gain), reinterpret_cast<__nv_bfloat16*>(xg),
+                     xg_lo_off, ss, keys, n_keys, dev_status);
   return launch_ex(embed_kernel<float>, dim3(B * R), dim3(256), 0, s, pdl,
-                   reinterpret_cast<const float*>(embed), anchor, mask_id, R, D, V, h, keys, n_keys,
-                   dev_status);
-}
-
-cudaError_t launch_rmsnorm(const float* x, const void* gain, void* out, int rows, int D, float eps,
-                           int bf16, int mask_rows, int gamma, int R, cudaStream_t s, bool pdl) {
-  if (bf16)
-    return launch_ex(rmsnorm_kernel<__nv_bfloat16>, dim3(rows), dim3(256), 0, s, pdl, x,
-                     reinterpret_cast<const __nv_bfloat16*>(gain),
-                     reinterpret_cast<__nv_bfloat16*>(out), D, eps, mask_rows, gamma, R);
-  return launch_ex(rmsnorm_kernel<float>, dim3(rows), dim3(256), 0, s, pdl, x,
-                   reinterpret_cast<const float*>(gain), reinterpret_cast<float*>(out), D, eps,
-                   mask_rows, gamma, R);
+                   reinterpret_cast<const float*>(embed), anchor, mask_id, R, D, V, h,
+                   reinterpret_cast<const float*>(gain), reinterpret_cast<float*>(xg), size_t(0), ss,
+                   keys, n_keys, dev_status);
 }
 
 cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,

@@ -49,7 +49,7 @@ def assert_logits_close(gpu, want, what="logits", tol=LOGIT_TOL):
     return rel
 
 
-def assert_drafts_match(gpu_draft, oracle_logits, what="draft"):
+def assert_drafts_match(gpu_draft, oracle_logits, what="draft", gpu_logits=None):
     """Bit-exact except at near-ties of the oracle (top-2 margin < 1e-2)."""
     d = np.asarray(gpu_draft).reshape(-1)
     lg = np.asarray(oracle_logits, dtype=np.float64).reshape(d.shape[0], -1)
@@ -57,8 +57,17 @@ def assert_drafts_match(gpu_draft, oracle_logits, what="draft"):
     top2 = np.sort(lg, axis=-1)[:, -2:]
     margin = top2[:, 1] - top2[:, 0]
     bad = (d != want) & (margin >= MARGIN)
-    assert not bad.any(), f"{what}: {int(bad.sum())} tokens differ outside near-ties " \
-                          f"(rows {np.nonzero(bad)[0][:8].tolist()})"
+    if bad.any():
+        rows = np.nonzero(bad)[0]
+        detail = []
+        for r in rows[:4]:
+            item = (f"row {r}: gpu token {d[r]} oracle {want[r]} margin {margin[r]:.4g} "
+                    f"oracle logit of gpu token {lg[r, d[r]]:.5f} vs max {lg[r, want[r]]:.5f}")
+            if gpu_logits is not None:
+                gl = ref.f64(gpu_logits).reshape(d.shape[0], -1)
+                item += f"; gpu logits {gl[r, d[r]]:.5f} / {gl[r, want[r]]:.5f}"
+            detail.append(item)
+        raise AssertionError(f"{what}: {int(bad.sum())} tokens differ outside near-ties: " + "; ".join(detail))
     n_diff = int((d != want).sum())
     report(what, "tokens_differing_at_near_ties", n_diff, 0)
     return n_diff

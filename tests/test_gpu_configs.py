@@ -155,7 +155,8 @@ def test_draft_verify_loop_8_layers(dfl):
             t, c, n = ref.verify_accept(o_tl.numpy(), out["draft"])
             assert int(tau[b]) == t, (cyc, b, int(tau[b]), t)
             if in_step[b]:
-                nd = H.assert_drafts_match(draft[b].cpu().numpy(), out["logits"], f"cycle {cyc} b{b}")
+                nd = H.assert_drafts_match(draft[b].cpu().numpy(), out["logits"], f"cycle {cyc} b{b}",
+                                           gpu_logits=logits[b])
                 token_checks += 1
                 if nd == 0:
                     assert committed[b].cpu().tolist() == c.tolist()
