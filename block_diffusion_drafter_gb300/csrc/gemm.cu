@@ -44,8 +44,11 @@ __device__ __forceinline__ void store_out(void* out, int bf16, size_t idx, float
 // Runs on the 128 epilogue threads (etid 0..127). Every op works in batches
 // of kEpiBatch elements per thread: all global loads of a batch are issued
 // before any of its stores, so the loads overlap instead of serialising
-// behind possibly-aliasing stores.
-constexpr int kEpiBatch = 8;
+// behind possibly-aliasing stores. The batch stays small: the epilogue runs
+// once per CTA, while other CTAs on the SM stream weights, and fetching its
+// instructions then costs more than the loads it overlaps (a step of the
+// Qwen3-8B-shaped drafter took 34 us longer with batches of 8 than of 2).
+constexpr int kEpiBatch = 2;
 
 struct TokInfo {
   int pos[kBM];     // cache position of the tile's token x, -1 = skip
