@@ -234,3 +234,117 @@ def verify_accept(target_logits, draft):
     committed[:a] = d[:a]
     committed[a] = t[a]
     return a + 1, committed, int(t[a])
+
+
+# -- NEXT: sampling (temperature > 0) draft and verification -------------------
+#
+# [P1] result tables "Qwen3-8B, temp 1" rows and [P2] "DFlash는 손실 없는 가속을
+# 보장한다" paragraph: at temperature 1 the draft is sampled and verified by
+# rejection-acceptance sampling, so the committed tokens follow the target's
+# own sampling distribution. The pages name the mechanism but print no
+# formula; the reading is standard speculative sampling:
+#   q_j = softmax(drafter logits_j / T), x_j ~ q_j;
+#   p_j = softmax(target logits_j / T);
+#   draft j is accepted while r_j * q_j(x_j) < p_j(x_j), r_j ~ U(0, 1);
+#   at the first rejection a the replacement is drawn from
+#   norm(max(p_a - q_a, 0)); if all gamma are accepted the bonus is drawn
+#   from p_gamma.
+# Categorical draws use the Gumbel-max rule: argmax_v (log w_v + g_v) with
+# g_v = -ln(-ln u_v) is a draw from w / sum(w).
+#
+# Random numbers: one counter-based generator, splitmix64 (Steele, Lea and
+# Flood, "Fast splittable pseudorandom number generators", 2014; Vigna's
+# reference splitmix64.c): the (c+1)-th output of the sequence started at
+# state `seed` is mix(seed + (c + 1) * 0x9E3779B97F4A7C15 mod 2^64). The
+# counter of a draw is c = stream * 2^60 + j * 2^52 + b * 2^32 + v, streams
+# 0 draft sample, 1 residual sample, 2 bonus sample, 3 acceptance uniform.
+# A uniform in (0, 1) is ((z >> 40) + 1/2) * 2^-24.
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+STREAM_DRAFT, STREAM_RESID, STREAM_BONUS, STREAM_ACCEPT = 0, 1, 2, 3
+
+
+def rng_u64(seed: int, stream: int, j: int, b: int, v) -> np.ndarray:
+    """splitmix64 outputs for counters (stream, j, b, v); v an int or array."""
+    with np.errstate(over="ignore"):
+        c = (np.uint64(stream) << np.uint64(60)) | (np.uint64(j) << np.uint64(52)) | \
+            (np.uint64(b) << np.uint64(32)) | np.asarray(v, dtype=np.uint64)
+        z = np.uint64(seed) + (c + np.uint64(1)) * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+
+def rng_uniform(seed: int, stream: int, j: int, b: int, v) -> np.ndarray:
+    """Uniform in (0, 1) with 24 random bits: ((z >> 40) + 0.5) / 2^24."""
+    z = rng_u64(seed, stream, j, b, v)
+    return ((z >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
+
+
+def gumbel(seed: int, stream: int, j: int, b: int, n: int) -> np.ndarray:
+    """Standard Gumbel noise -ln(-ln u) for v = 0 .. n-1."""
+    u = rng_uniform(seed, stream, j, b, np.arange(n, dtype=np.uint64))
+    return -np.log(-np.log(u))
+
+
+def softmax_t(logits: np.ndarray, T: float) -> np.ndarray:
+    """softmax(logits / T) over the last axis, by max subtraction."""
+    z = f64(logits) / T
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def gumbel_argmax(score: np.ndarray, g: np.ndarray) -> int:
+    """Categorical draw by the Gumbel-max rule over entries with finite score
+    (score = log weight, -inf for weight 0); ties -> lowest index."""
+    return int(np.argmax(score + g))
+
+
+def draft_sample(logits, T: float, seed: int, b: int) -> np.ndarray:
+    """Draft tokens x_j ~ softmax(logits_j / T) for mask rows j = 0..gamma-1
+    of sequence b (stream 0)."""
+    lg = f64(logits)
+    V = lg.shape[-1]
+    return np.array([gumbel_argmax(lg[j] / T, gumbel(seed, STREAM_DRAFT, j, b, V))
+                     for j in range(lg.shape[0])], dtype=np.int64)
+
+
+def accept_probability(p: np.ndarray, q: np.ndarray, x: int) -> float:
+    """min(1, p(x) / q(x)): the chance that draft x, drawn from q, is kept."""
+    return 1.0 if q[x] <= p[x] else p[x] / q[x]
+
+
+def residual_distribution(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """norm(max(p - q, 0)); p itself when p == q everywhere (no residual mass)."""
+    w = np.maximum(p - q, 0.0)
+    s = w.sum()
+    return w / s if s > 0 else p
+
+
+def verify_sample(target_logits, draft_logits, draft, T: float, seed: int, b: int):
+    """Rejection-acceptance verification of one block of sequence b.
+    target_logits [gamma+1, V] (row j: target distribution after the anchor
+    and draft[0..j-1]); draft_logits [gamma, V]; draft [gamma].
+    Returns (tau, committed [gamma+1] padded with -1, next_anchor)."""
+    p = softmax_t(target_logits, T)
+    q = softmax_t(draft_logits, T)
+    d = np.asarray(draft)
+    gamma, V = d.shape[0], p.shape[-1]
+    a = 0
+    while a < gamma:
+        r = float(rng_uniform(seed, STREAM_ACCEPT, a, b, 0))
+        if r * q[a, d[a]] < p[a, d[a]]:
+            a += 1
+        else:
+            break
+    if a < gamma:
+        w = residual_distribution(p[a], q[a])
+        with np.errstate(divide="ignore"):
+            y = gumbel_argmax(np.log(w), gumbel(seed, STREAM_RESID, a, b, V))
+    else:
+        y = gumbel_argmax(f64(target_logits)[gamma] / T, gumbel(seed, STREAM_BONUS, gamma, b, V))
+    committed = np.full(gamma + 1, -1, dtype=np.int64)
+    committed[:a] = d[:a]
+    committed[a] = y
+    return a + 1, committed, int(y)

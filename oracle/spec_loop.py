@@ -145,3 +145,52 @@ def speculative_generate(target: TinyTarget, drafter, prompt, n_new: int,
         out.extend(int(x) for x in committed[:tau])
         anchor = nxt
     return out[:n_new]
+
+
+def cycle_seed(seed: int, cycle: int) -> int:
+    """Per-cycle generator state: a splitmix64 output of (seed, cycle), so
+    that every cycle draws from its own counter space."""
+    return int(ref.rng_u64(seed, 15, 0, 0, cycle))
+
+
+def speculative_sample_generate(target: TinyTarget, draft_logits_fn, prompt, anchor: int,
+                                n_new: int, gamma: int, T: float, seed: int,
+                                stats: list | None = None) -> list[int]:
+    """Speculative decoding at temperature T from a given anchor ([P1] temp-1
+    results; [P2] lossless rejection-acceptance paragraph): each cycle the
+    drafter's logits [gamma, V] give sampled drafts (ref.draft_sample), the
+    target scores [anchor, drafts] in one pass, and ref.verify_sample commits
+    tau tokens. draft_logits_fn(anchor, seq) may be any drafter: the
+    committed stream follows the target's sampling distribution regardless.
+    Returns the first n_new committed tokens after the anchor."""
+    seq = list(prompt)
+    out = []
+    cycle = 0
+    while len(out) < n_new:
+        s = cycle_seed(seed, cycle)
+        ql = ref.f64(draft_logits_fn(anchor, seq))
+        d = ref.draft_sample(ql, T, s, 0)
+        block = seq + [anchor] + [int(x) for x in d]
+        logits, _ = target.forward(block)
+        n0 = len(seq)
+        tau, committed, nxt = ref.verify_sample(logits[n0:n0 + gamma + 1], ql, d, T, s, 0)
+        if stats is not None:
+            stats.append(tau)
+        seq = seq + [anchor] + [int(x) for x in d[: tau - 1]]
+        out.extend(int(x) for x in committed[:tau])
+        anchor = nxt
+        cycle += 1
+    return out[:n_new]
+
+
+def target_sampling_pair_probs(target: TinyTarget, prompt, anchor: int, T: float) -> np.ndarray:
+    """Exact P(first two tokens after the anchor = (y1, y2)) under target-only
+    sampling at temperature T: p(y1 | prompt, anchor) * p(y2 | ..., y1)."""
+    base = list(prompt) + [anchor]
+    logits, _ = target.forward(base)
+    p1 = ref.softmax_t(logits[-1], T)
+    P = np.zeros((target.V, target.V))
+    for y1 in range(target.V):
+        l2, _ = target.forward(base + [y1])
+        P[y1] = p1[y1] * ref.softmax_t(l2[-1], T)
+    return P
