@@ -258,7 +258,7 @@ def verify_accept(target_logits, draft):
 # state `seed` is mix(seed + (c + 1) * 0x9E3779B97F4A7C15 mod 2^64). The
 # counter of a draw is c = stream * 2^60 + j * 2^52 + b * 2^32 + v, streams
 # 0 draft sample, 1 residual sample, 2 bonus sample, 3 acceptance uniform.
-# A uniform in (0, 1) is ((z >> 40) + 1/2) * 2^-24.
+# A uniform in (0, 1) is ((z >> 41) + 1/2) * 2^-23 (exact in float32).
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 STREAM_DRAFT, STREAM_RESID, STREAM_BONUS, STREAM_ACCEPT = 0, 1, 2, 3
@@ -276,9 +276,10 @@ def rng_u64(seed: int, stream: int, j: int, b: int, v) -> np.ndarray:
 
 
 def rng_uniform(seed: int, stream: int, j: int, b: int, v) -> np.ndarray:
-    """Uniform in (0, 1) with 24 random bits: ((z >> 40) + 0.5) / 2^24."""
+    """Uniform in (0, 1) with 23 random bits: ((z >> 41) + 0.5) / 2^23, a
+    value float32 holds exactly."""
     z = rng_u64(seed, stream, j, b, v)
-    return ((z >> np.uint64(40)).astype(np.float64) + 0.5) / float(1 << 24)
+    return ((z >> np.uint64(41)).astype(np.float64) + 0.5) / float(1 << 23)
 
 
 def gumbel(seed: int, stream: int, j: int, b: int, n: int) -> np.ndarray:

@@ -59,7 +59,8 @@ def test_counter_form_equals_the_sequential_generator():
 def test_uniforms_lie_strictly_inside_the_unit_interval_and_are_flat():
     u = ref.rng_uniform(99, 3, 0, 0, np.arange(1 << 16, dtype=np.uint64))
     assert u.min() > 0.0 and u.max() < 1.0
-    assert np.all(u * (1 << 24) - 0.5 == np.floor(u * (1 << 24)))   # 24-bit grid + 1/2
+    assert np.all(u * (1 << 23) - 0.5 == np.floor(u * (1 << 23)))   # 23-bit grid + 1/2
+    assert np.all(u.astype(np.float32).astype(np.float64) == u)      # exact in float32
     counts = np.histogram(u, bins=32, range=(0, 1))[0]
     assert chi2_pvalue(counts, np.full(32, 1 / 32)) > 1e-3
 
