@@ -72,6 +72,11 @@ _SIGS = {
     "dflash_rope_tables": (_I, [ctypes.POINTER(Config), _I, _P, _P]),
     "dflash_linear": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "dflash_verify_accept_noalloc": (_I, [ctypes.POINTER(Config), _P, _I, _P, _I, _P, _P, _P, _P]),
+    "dflash_draft_block_sample": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P,
+                                       _I, _I, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P,
+                                       _P, _SZ, ctypes.POINTER(Trace), _P]),
+    "dflash_verify_sample": (_I, [ctypes.POINTER(Config), _P, _I, _P, _P, _I, ctypes.c_float,
+                                  ctypes.c_uint64, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
 }
 
 _lib = None
@@ -243,6 +248,30 @@ def dflash_verify_accept(cfg, target_logits, draft, tau, committed, next_anchor,
         ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), B, _ptr(tau), _ptr(committed),
         _ptr(next_anchor), ws.ptr, ws.nbytes,
         ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_draft_block_sample(cfg, w: Weights, anchor, ctx_len, max_ctx_hint, k_cache, v_cache,
+                              temperature, seed, draft, logits, dev_status, ws: Workspace, trace=None,
+                              stream=None):
+    """Sampling drafting pass: draft j ~ softmax(logits_j / temperature);
+    logits [B, gamma, V] fp32 receives the raw logits (the verifier's q)."""
+    B = anchor.shape[0]
+    _check("dflash_draft_block_sample", load().dflash_draft_block_sample(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(anchor), _ptr(ctx_len), B,
+        int(max_ctx_hint), _ptr(k_cache), _ptr(v_cache), float(temperature), int(seed) & (2**64 - 1),
+        _ptr(draft), _ptr(logits), _ptr(dev_status), ws.ptr, ws.nbytes,
+        ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_verify_sample(cfg, target_logits, draft_logits, draft, temperature, seed, tau, committed,
+                         next_anchor, ws: Workspace, trace=None, stream=None):
+    """Rejection-acceptance verification at temperature > 0."""
+    dt = BF16 if target_logits.dtype == torch.bfloat16 else F32
+    B = target_logits.shape[0]
+    _check("dflash_verify_sample", load().dflash_verify_sample(
+        ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft_logits), _ptr(draft), B,
+        float(temperature), int(seed) & (2**64 - 1), _ptr(tau), _ptr(committed), _ptr(next_anchor),
+        ws.ptr, ws.nbytes, ctypes.byref(trace) if trace is not None else None, _stream(stream)))
 
 
 def dflash_verify_accept_noalloc(cfg, target_logits, draft, tau, committed, next_anchor,

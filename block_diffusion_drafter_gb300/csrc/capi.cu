@@ -2,6 +2,7 @@
 // launch sequences of dflash_ctx_fuse / dflash_kv_inject / dflash_draft_block
 // / dflash_verify_accept. Host code only; every step of the path runs in the
 // kernels of gemm.cu, attention.cu and small.cu.
+#include <cmath>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -17,7 +18,7 @@ inline int elem_bytes(const dflash_config* c) { return c->dtype == DFLASH_BF16 ?
 inline int rows_per_block(const dflash_config* c) { return c->gamma + 1; }
 
 struct WsLayout {
-  size_t h, xn, q, attn_o, act, z, ss, lm_keys, v_keys, v_count;
+  size_t h, xn, q, attn_o, act, z, ss, lm_keys, v_keys, v_count, samp;
   size_t row_ss;
   size_t fixed;  // bytes before row_ss
 };
@@ -43,6 +44,7 @@ WsLayout ws_layout(const dflash_config* c) {
   L.lm_keys = take(static_cast<size_t>(c->max_batch) * c->gamma * 8);
   L.v_keys = take(rows * 8);
   L.v_count = take(static_cast<size_t>(c->max_batch) * 4);
+  L.samp = take(dfl::sample_ws_bytes(c->max_batch, c->gamma, c->vocab));
   L.row_ss = off;
   L.fixed = off;
   return L;
@@ -464,11 +466,11 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
 
 extern "C" {
 
-dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
-                                 const int32_t* ctx_len, int B, int max_ctx_hint, void* k_cache,
-                                 void* v_cache, int32_t* draft, float* logits_opt,
-                                 float* layer_dump_opt, int32_t* dev_status, void* ws, size_t ws_bytes,
-                                 dflash_trace* trace, dflash_stream_t stream) {
+static dflash_status draft_block_impl(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
+                                      const int32_t* ctx_len, int B, int max_ctx_hint, void* k_cache,
+                                      void* v_cache, float temperature, uint64_t seed, int32_t* draft,
+                                      float* logits_opt, float* layer_dump_opt, int32_t* dev_status, void* ws,
+                                      size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
   if (w == nullptr || B < 1 || B > c->max_batch || max_ctx_hint < 0) return DFLASH_ERR_INVALID_ARG;
@@ -684,6 +686,9 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
     g.epi = base_epi(c);
     g.epi.op = EPI_ARGMAX; g.epi.out = logits_opt; g.epi.ld = V; g.epi.n_tok = nmask; g.epi.n_feat = V;
     g.epi.keys = keys;
+    g.epi.gamma = c->gamma;
+    g.epi.temperature = temperature;
+    g.epi.seed = seed;
     fold_in(g.epi);
     const double b = (static_cast<double>(V) * D + static_cast<double>(nmask) * D) * es;
     if ((st = run_gemm(cx, g, m_lm, m_z, p_lm, b, 2.0 * nmask * V * static_cast<double>(D))) != DFLASH_OK)
@@ -693,6 +698,57 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
   st = fail(launch_argmax_finalize(keys, nmask, draft, cx.s, cx.pdl));
   cx.tr.after();
   return st;
+}
+
+dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
+                                 const int32_t* ctx_len, int B, int max_ctx_hint, void* k_cache,
+                                 void* v_cache, int32_t* draft, float* logits_opt,
+                                 float* layer_dump_opt, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                 dflash_trace* trace, dflash_stream_t stream) {
+  return draft_block_impl(c, w, anchor, ctx_len, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+                          logits_opt, layer_dump_opt, dev_status, ws, ws_bytes, trace, stream);
+}
+
+dflash_status dflash_draft_block_sample(const dflash_config* c, const dflash_weights* w,
+                                        const int32_t* anchor, const int32_t* ctx_len, int B,
+                                        int max_ctx_hint, void* k_cache, void* v_cache, float temperature,
+                                        uint64_t seed, int32_t* draft, float* logits,
+                                        int32_t* dev_status, void* ws, size_t ws_bytes,
+                                        dflash_trace* trace, dflash_stream_t stream) {
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || logits == nullptr) return DFLASH_ERR_INVALID_ARG;
+  return draft_block_impl(c, w, anchor, ctx_len, B, max_ctx_hint, k_cache, v_cache, temperature, seed, draft,
+                          logits, nullptr, dev_status, ws, ws_bytes, trace, stream);
+}
+
+dflash_status dflash_verify_sample(const dflash_config* c, const void* target_logits,
+                                   dflash_dtype logits_dtype, const float* draft_logits,
+                                   const int32_t* draft, int B, float temperature, uint64_t seed,
+                                   int32_t* tau, int32_t* committed, int32_t* next_anchor, void* ws,
+                                   size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
+  dflash_status st = dflash_check_config(c);
+  if (st != DFLASH_OK) return st;
+  if (logits_dtype != DFLASH_BF16 && logits_dtype != DFLASH_F32) return DFLASH_ERR_DTYPE;
+  if (B < 1 || B > c->max_batch || target_logits == nullptr || draft_logits == nullptr ||
+      draft == nullptr || tau == nullptr || committed == nullptr || next_anchor == nullptr ||
+      !(temperature > 0.f) || !std::isfinite(temperature))
+    return DFLASH_ERR_INVALID_ARG;
+  if (!trace_ok(trace)) return DFLASH_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c);
+  if (ws == nullptr || ws_bytes < L.fixed) return DFLASH_ERR_WORKSPACE;
+  if ((st = check_arch()) != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Tracer tr{trace, s};
+  const int R = c->gamma + 1;
+  // target rows once and drafter rows once for the statistics, then row a of each for the draw
+  const double row = static_cast<double>(c->vocab);
+  const double bytes = B * (R * row * (logits_dtype == DFLASH_BF16 ? 2 : 4) + c->gamma * row * 4 +
+                            row * ((logits_dtype == DFLASH_BF16 ? 2 : 4) + 4));
+  tr.before(DFLASH_K_VERIFY, bytes, 0);
+  const cudaError_t e = launch_sample_verify(target_logits, logits_dtype == DFLASH_BF16, draft_logits, draft,
+                                             B, c->gamma, c->vocab, temperature, seed, at<void>(ws, L.samp),
+                                             tau, committed, next_anchor, s, use_pdl());
+  tr.after();
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
 dflash_status dflash_verify_accept(const dflash_config* c, const void* target_logits,

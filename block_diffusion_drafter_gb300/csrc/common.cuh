@@ -283,4 +283,30 @@ __device__ __forceinline__ uint32_t argmax_key_index(unsigned long long k) {
   return 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
 }
 
+// ----------------------------------------------------------------- sampling RNG
+// Counter-based splitmix64 (Steele, Lea and Flood 2014; Vigna's splitmix64.c):
+// the (c+1)-th output of the generator started at state `seed`. A draw's
+// counter is stream << 60 | j << 52 | b << 32 | v (stream 0 draft sample,
+// 1 residual sample, 2 bonus sample, 3 acceptance uniform; j position in the
+// block, b sequence, v vocabulary index).
+constexpr int kStreamDraft = 0, kStreamResid = 1, kStreamBonus = 2, kStreamAccept = 3;
+__device__ __forceinline__ uint64_t rng_counter(int stream, int j, int b, uint32_t v) {
+  return (static_cast<uint64_t>(stream) << 60) | (static_cast<uint64_t>(j) << 52) |
+         (static_cast<uint64_t>(b) << 32) | static_cast<uint64_t>(v);
+}
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t counter) {
+  uint64_t z = seed + (counter + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+// Uniform in (0, 1): ((z >> 41) + 1/2) * 2^-23, exact in fp32.
+__device__ __forceinline__ float rng_uniform(uint64_t seed, uint64_t counter) {
+  return (static_cast<float>(splitmix64_at(seed, counter) >> 41) + 0.5f) * (1.0f / 8388608.0f);
+}
+// Standard Gumbel noise -ln(-ln u): argmax_v (log w_v + g_v) draws v from w / sum(w).
+__device__ __forceinline__ float rng_gumbel(uint64_t seed, uint64_t counter) {
+  return -logf(-logf(rng_uniform(seed, counter)));
+}
+
 }  // namespace dfl

@@ -334,7 +334,13 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           const int feat = m_tile * kBM + a;
           if (feat < e.n_feat) {
             const float v = S[b * kSLD + a] * (e.ss_in != nullptr ? rstd[b] : 1.f);
-            const unsigned long long key = argmax_key(v, static_cast<uint32_t>(feat));
+            // sampling: rank by v / T + Gumbel noise (a draw from softmax(v / T))
+            const float rank = e.temperature > 0.f && tok < e.n_tok
+                                   ? v / e.temperature +
+                                         rng_gumbel(e.seed, rng_counter(kStreamDraft, tok % e.gamma, tok / e.gamma,
+                                                                        static_cast<uint32_t>(feat)))
+                                   : v;
+            const unsigned long long key = argmax_key(rank, static_cast<uint32_t>(feat));
             best = key > best ? key : best;
             if (e.out != nullptr && tok < e.n_tok)
               reinterpret_cast<float*>(e.out)[static_cast<size_t>(tok) * e.ld + feat] = v;

@@ -46,6 +46,10 @@ struct Epi {
   int rope_positions;
   // EPI_ARGMAX
   unsigned long long* keys;
+  // EPI_ARGMAX sampling mode (temperature > 0): token t = b * gamma + j ranks
+  // vocabulary entry v by logit / temperature + Gumbel(seed, stream 0, j, b, v)
+  float temperature;
+  uint64_t seed;
   // EPI_FUSE
   float* row_ss;      // [n_tok, n_ss] partial sums of squares
   int n_ss;
@@ -146,6 +150,22 @@ cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int 
 // h[t] = gain * u[t] / sqrt(sum(row_ss[t]) / D + eps), u fp32, h in cfg dtype.
 cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
                              int T, int D, float eps, int bf16, cudaStream_t s, bool pdl);
+// Sampling verification (temperature > 0): rejection-acceptance over the
+// target logits [B, gamma+1, V] (bf16 or fp32) and the drafter logits
+// [B, gamma, V] (fp32) of the sampled drafts. Three launches: per-chunk
+// softmax statistics of every row, the acceptance scan (one CTA per
+// sequence), and the residual / bonus draw over V with the decision.
+constexpr int kSampChunk = 4096;  // vocabulary entries per statistics CTA
+struct SampleState {
+  int a;                 // accepted drafts
+  float mt, st, md, sd;  // softmax max and sum (of logit / T) of target and draft row a
+  int pad[3];
+};
+size_t sample_ws_bytes(int max_batch, int gamma, int vocab);
+cudaError_t launch_sample_verify(const void* target, int target_bf16, const float* draft_logits,
+                                 const int32_t* draft, int B, int gamma, int V, float temperature,
+                                 uint64_t seed, void* ws, int32_t* tau, int32_t* committed,
+                                 int32_t* next_anchor, cudaStream_t s, bool pdl);
 cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int32_t* draft,
                                    cudaStream_t s, bool pdl);
 cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,

@@ -220,6 +220,52 @@ dflash_status dflash_draft_block(const dflash_config* cfg, const dflash_weights*
                                  void* ws, size_t ws_bytes, dflash_trace* trace,
                                  dflash_stream_t stream);
 
+/* Sampling mode of the drafting pass (temperature > 0): the pass of
+ * dflash_draft_block, except that draft token j of sequence b is a draw from
+ * softmax(logits_j / temperature) (the temperature-1 setting of [P1] result
+ * tables and [P2]'s lossless rejection-acceptance paragraph), by the
+ * Gumbel-max rule: draft = argmax_v (logit_v / T + G_v), G_v = -ln(-ln u_v),
+ * u_v = ((z >> 41) + 1/2) 2^-23 with z the splitmix64 output (Steele, Lea,
+ * Flood 2014; Vigna's splitmix64.c) of state `seed` at counter
+ *   0 << 60 | j << 52 | b << 32 | v          (stream 0: draft sample).
+ * logits: device fp32 [B, gamma, V], required: the raw logits (not divided by
+ *   T), which dflash_verify_sample needs as the drafter distribution q.
+ * Other arguments as in dflash_draft_block (no layer dump). Returns
+ * DFLASH_ERR_INVALID_ARG for temperature <= 0 or not finite, or logits NULL. */
+dflash_status dflash_draft_block_sample(const dflash_config* cfg, const dflash_weights* w,
+                                        const int32_t* anchor, const int32_t* ctx_len, int B,
+                                        int max_ctx_hint, void* k_cache, void* v_cache,
+                                        float temperature, uint64_t seed, int32_t* draft,
+                                        float* logits, int32_t* dev_status, void* ws,
+                                        size_t ws_bytes, dflash_trace* trace,
+                                        dflash_stream_t stream);
+
+/* Sampling verification (temperature > 0) by rejection-acceptance, which
+ * keeps the committed tokens distributed as the target's own sampling
+ * ([P2] lossless paragraph; reading: standard speculative sampling):
+ *   p_j = softmax(target_logits[b, j] / T),  q_j = softmax(draft_logits[b, j] / T)
+ *   for j = 0..gamma-1: keep draft j while u_j q_j(x_j) < p_j(x_j), u_j the
+ *     uniform of stream 3 at counter 3 << 60 | j << 52 | b << 32 | 0;
+ *   a = kept drafts; tau[b] = a + 1;
+ *   a < gamma: y = argmax_v (ln max(p_a(v) - q_a(v), 0) + G_v), stream 1 at
+ *     (j = a, v) (entries with no residual mass excluded; if none has mass,
+ *     y = argmax_v (target_logits[b, a, v] / T + G_v), same noise);
+ *   a = gamma: y = argmax_v (target_logits[b, gamma, v] / T + G_v), stream 2
+ *     at (j = gamma, v);
+ *   committed[b] = draft[b, 0..a-1] ++ [y] ++ (-1 padding); next_anchor[b] = y.
+ * Same generator and uniform as dflash_draft_block_sample. Ties of a draw go
+ * to the lowest index. A draft id outside [0, V) counts as rejected.
+ * target_logits: device [B, gamma+1, V] of logits_dtype;
+ * draft_logits: device fp32 [B, gamma, V] (dflash_draft_block_sample's logits);
+ * draft: device [B, gamma]; tau, next_anchor: device [B]; committed: device
+ * [B, gamma+1]. Three launches; the workspace holds their scratch. */
+dflash_status dflash_verify_sample(const dflash_config* cfg, const void* target_logits,
+                                   dflash_dtype logits_dtype, const float* draft_logits,
+                                   const int32_t* draft, int B, float temperature,
+                                   uint64_t seed, int32_t* tau, int32_t* committed,
+                                   int32_t* next_anchor, void* ws, size_t ws_bytes,
+                                   dflash_trace* trace, dflash_stream_t stream);
+
 /* Greedy verification, [P1] "Preliminaries" eq. (1) (tau in [1, gamma+1],
  * bonus token included) and "추론 구조" (the target verifies the block):
  *   t_j = argmax_V target_logits[b, j]   (j = 0..gamma; lowest index on ties)

@@ -116,3 +116,29 @@ def test_null_arguments_rejected_before_any_launch(lib):
     assert L.dflash_verify_accept(ctypes.byref(cfg), 1, 0, 1, cfg.max_batch + 1, 1, 1, 1, 1, 1,
                                   None, None) == lib.ERR_INVALID_ARG
     assert L.dflash_linear(5, None, None, None, 1, 1, 64, None, 0, None) == lib.ERR_DTYPE
+
+
+def test_sampling_entry_points_reject_bad_arguments_before_any_launch(lib):
+    L = lib.load()
+    cfg = lib.config_from_workload(synth.WORKLOADS["tiny_f32_L1_N128"])
+    w = lib.WeightsStruct()
+    fake = 256  # any non-null address: nothing is dereferenced on the host
+    # temperature must be > 0 and finite; the logits buffer is required
+    for t in (0.0, -1.0, float("inf"), float("nan")):
+        assert L.dflash_draft_block_sample(ctypes.byref(cfg), ctypes.byref(w), fake, fake, 1, 0, fake, fake,
+                                           t, 1, fake, fake, fake, fake, 1 << 30, None,
+                                           None) == lib.ERR_INVALID_ARG
+        assert L.dflash_verify_sample(ctypes.byref(cfg), fake, lib.F32, fake, fake, 1, t, 1, fake, fake,
+                                      fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_draft_block_sample(ctypes.byref(cfg), ctypes.byref(w), fake, fake, 1, 0, fake, fake,
+                                       1.0, 1, fake, None, fake, fake, 1 << 30, None,
+                                       None) == lib.ERR_INVALID_ARG
+    assert L.dflash_verify_sample(ctypes.byref(cfg), fake, lib.F32, None, fake, 1, 1.0, 1, fake, fake, fake,
+                                  fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_verify_sample(ctypes.byref(cfg), fake, 7, fake, fake, 1, 1.0, 1, fake, fake, fake,
+                                  fake, 1 << 30, None, None) == lib.ERR_DTYPE
+    assert L.dflash_verify_sample(ctypes.byref(cfg), fake, lib.F32, fake, fake, cfg.max_batch + 1, 1.0, 1,
+                                  fake, fake, fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+    # workspace too small
+    assert L.dflash_verify_sample(ctypes.byref(cfg), fake, lib.F32, fake, fake, 1, 1.0, 1, fake, fake, fake,
+                                  fake, 16, None, None) == lib.ERR_WORKSPACE
