@@ -154,7 +154,8 @@ class DraftCycle:
         self.max_ctx = int(synth.ctx_lengths(wl).max())
         torch.cuda.synchronize()
 
-    def step(self, trace=None):
+    def step_draft(self, trace=None):
+        """Fusion and injection of the step's new rows, then the drafting pass."""
         d, wl = self.dfl, self.wl
         self.ctx_len.copy_(self.ctx0)
         d.dflash_ctx_fuse(self.cfg, self.w, self.step_taps, self.h_new.view(-1, wl.d_model), self.ws,
@@ -163,8 +164,14 @@ class DraftCycle:
                            self.v_cache, self.status, self.ws, trace=trace)
         d.dflash_draft_block(self.cfg, self.w, self.anchor, self.ctx_len, self.max_ctx, self.k_cache,
                              self.v_cache, self.draft, self.status, self.ws, trace=trace)
-        d.dflash_verify_accept(self.cfg, self.target, self.draft, self.tau, self.committed,
-                               self.next_anchor, self.ws, trace=trace)
+
+    def step_verify(self, trace=None):
+        self.dfl.dflash_verify_accept(self.cfg, self.target, self.draft, self.tau, self.committed,
+                                      self.next_anchor, self.ws, trace=trace)
+
+    def step(self, trace=None):
+        self.step_draft(trace)
+        self.step_verify(trace)
 
     def launches_per_step(self) -> int:
         rec = self.dfl.TraceRecorder(256)
@@ -364,14 +371,34 @@ def run_gpu(args):
     o_tau = torch.empty_like(cyc.tau, device="cpu").pin_memory()
     o_comm = torch.empty_like(cyc.committed, device="cpu").pin_memory()
 
-    def e2e_step():
+    def e2e_body():
+        # the step's target logits are needed only by verification: their H2D
+        # runs on a second stream while fusion, injection and drafting run
+        cur = torch.cuda.current_stream()
+        copy_stream.wait_stream(cur)
+        with torch.cuda.stream(copy_stream):
+            cyc.target.copy_(h_target, non_blocking=True)
         cyc.step_taps.copy_(h_taps, non_blocking=True)
-        cyc.target.copy_(h_target, non_blocking=True)
         cyc.anchor.copy_(h_anchor, non_blocking=True)
-        fn()
+        cyc.step_draft()
+        cur.wait_stream(copy_stream)
+        cyc.step_verify()
         o_draft.copy_(cyc.draft, non_blocking=True)
         o_tau.copy_(cyc.tau, non_blocking=True)
         o_comm.copy_(cyc.committed, non_blocking=True)
+
+    copy_stream = torch.cuda.Stream()
+    e2e_step = e2e_body
+    if graph is not None:   # the same copies and launches, captured once and replayed
+        try:
+            e2e_body()
+            torch.cuda.synchronize()
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e):
+                e2e_body()
+            e2e_step = g_e2e.replay
+        except Exception:
+            e2e_step = e2e_body
 
     for _ in range(3):
         e2e_step()

@@ -583,8 +583,10 @@ __global__ void __launch_bounds__(kGemmThreads)
     // cluster rank = split). After the barrier every partial is visible;
     // CTA r reduces the token columns [c0, c1) of the tile by reading the
     // partials of all splits through distributed shared memory, in ascending
-    // split order, then runs the epilogue on them. The second barrier keeps
-    // every partial alive until all peers have read it.
+    // split order, then runs the epilogue on them. A second barrier keeps
+    // every partial alive until all peers have read it: each CTA arrives as
+    // soon as its reads are done and waits only at the very end, so the
+    // epilogue runs while slower peers finish reading.
     cluster_sync();
     if (warp >= 2) {
       const int etid = threadIdx.x - 64;
@@ -595,6 +597,7 @@ __global__ void __launch_bounds__(kGemmThreads)
       const uint32_t p_local = tiles_s;
       float* S = reinterpret_cast<float*>(tiles + static_cast<size_t>(g.bn) * kBM * 4);
       const bool ok = hdr->epi_ok != 0;
+      bool arrived = false;
       for (int cb = c0; cb < c1; cb += kBM) {
         const int cols = min(kBM, c1 - cb);
         if (ok) {
@@ -614,11 +617,18 @@ __global__ void __launch_bounds__(kGemmThreads)
           }
         }
         named_bar(1, 128);
+        if (cb + kBM >= c1) {  // the last reads of peer partials are done
+          cluster_arrive();
+          arrived = true;
+        }
         if (ok) apply_epilogue<kOp>(g, S, &hdr->tok, cb, cols, m_tile, n_tile, etid);
         named_bar(1, 128);
       }
+      if (!arrived) cluster_arrive();
+    } else {
+      cluster_arrive();
     }
-    cluster_sync();
+    cluster_wait();
   }
   __syncthreads();
   if (warp == 1) {
