@@ -72,6 +72,10 @@ _SIGS = {
     "dflash_rope_tables": (_I, [ctypes.POINTER(Config), _I, _P, _P]),
     "dflash_linear": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "dflash_verify_accept_noalloc": (_I, [ctypes.POINTER(Config), _P, _I, _P, _I, _P, _P, _P, _P]),
+    "dflash_draft_block_dyn": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _P,
+                                    _I, _I, _P, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
+    "dflash_verify_accept_dyn": (_I, [ctypes.POINTER(Config), _P, _I, _P, _P, _I, _P, _P, _P, _P, _SZ,
+                                      ctypes.POINTER(Trace), _P]),
     "dflash_draft_block_sample": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P,
                                        _I, _I, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P,
                                        _P, _SZ, ctypes.POINTER(Trace), _P]),
@@ -247,6 +251,27 @@ def dflash_verify_accept(cfg, target_logits, draft, tau, committed, next_anchor,
     _check("dflash_verify_accept", load().dflash_verify_accept(
         ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), B, _ptr(tau), _ptr(committed),
         _ptr(next_anchor), ws.ptr, ws.nbytes,
+        ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_draft_block_dyn(cfg, w: Weights, anchor, ctx_len, gamma_b, max_ctx_hint, k_cache, v_cache,
+                           draft, dev_status, ws: Workspace, logits=None, trace=None, stream=None):
+    """Drafting pass with block size gamma_b[b] per sequence (draft[b, j] = -1
+    for j >= gamma_b[b])."""
+    B = anchor.shape[0]
+    _check("dflash_draft_block_dyn", load().dflash_draft_block_dyn(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(anchor), _ptr(ctx_len), _ptr(gamma_b), B,
+        int(max_ctx_hint), _ptr(k_cache), _ptr(v_cache), _ptr(draft), _ptr(logits), _ptr(dev_status),
+        ws.ptr, ws.nbytes, ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_verify_accept_dyn(cfg, target_logits, draft, gamma_b, tau, committed, next_anchor,
+                             ws: Workspace, trace=None, stream=None):
+    dt = BF16 if target_logits.dtype == torch.bfloat16 else F32
+    B = target_logits.shape[0]
+    _check("dflash_verify_accept_dyn", load().dflash_verify_accept_dyn(
+        ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), _ptr(gamma_b), B, _ptr(tau),
+        _ptr(committed), _ptr(next_anchor), ws.ptr, ws.nbytes,
         ctypes.byref(trace) if trace is not None else None, _stream(stream)))
 
 

@@ -30,7 +30,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
   const int G = p.n_q_heads / p.n_kv_heads, kvh = hq / G;
   pdl_launch_dependents();
   pdl_wait();
-  const int n_keys = p.ctx_len[b] + p.R;
+  const int r_b = p.gamma_b == nullptr ? p.R : min(max(p.gamma_b[b], 1), p.R - 1) + 1;
+  const int n_keys = p.ctx_len[b] + r_b;
   const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
   const float* q = reinterpret_cast<const float*>(p.q) + (static_cast<size_t>(b) * p.R + i) * hq_stride + hq * DH;
   const size_t kv_base = (static_cast<size_t>(b) * p.n_kv_heads + kvh) * p.ncap * DH;

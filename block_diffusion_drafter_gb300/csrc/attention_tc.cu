@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   pdl_launch_dependents();
   pdl_wait();
 
-  const int n_keys = p.ctx_len[b] + p.R;
+  // the block's keys: rows 0..gamma_b[b] (clamped to the block), else all R
+  const int r_b = p.gamma_b == nullptr ? p.R : min(max(p.gamma_b[b], 1), p.R - 1) + 1;
+  const int n_keys = p.ctx_len[b] + r_b;
   const int k_begin = sp * p.chunk;
   const int k_end = (sp == p.splits - 1) ? n_keys : min(n_keys, (sp + 1) * p.chunk);
   const int nt = k_end > k_begin ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;

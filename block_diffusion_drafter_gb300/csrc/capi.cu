@@ -467,7 +467,8 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
 extern "C" {
 
 static dflash_status draft_block_impl(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
-                                      const int32_t* ctx_len, int B, int max_ctx_hint, void* k_cache,
+                                      const int32_t* ctx_len, const int32_t* gamma_b, int B,
+                                      int max_ctx_hint, void* k_cache,
                                       void* v_cache, float temperature, uint64_t seed, int32_t* draft,
                                       float* logits_opt, float* layer_dump_opt, int32_t* dev_status, void* ws,
                                       size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
@@ -614,7 +615,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
       a.v_cache = v_cache;
       a.layer = l;
       a.n_layers = Lyr;
-      a.ctx_len = ctx_len; a.out = ao;
+      a.ctx_len = ctx_len; a.gamma_b = gamma_b; a.out = ao;
       a.out_lo_off = ao_lo;
       a.dev_status = dev_status;
       a.B = B; a.R = R; a.n_q_heads = c->n_q_heads; a.n_kv_heads = c->n_kv_heads;
@@ -695,7 +696,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
       return st;
   }
   cx.tr.before(DFLASH_K_ARGMAX, nmask * 12.0, 0);
-  st = fail(launch_argmax_finalize(keys, nmask, draft, cx.s, cx.pdl));
+  st = fail(launch_argmax_finalize(keys, nmask, c->gamma, gamma_b, draft, cx.s, cx.pdl));
   cx.tr.after();
   return st;
 }
@@ -705,8 +706,18 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
                                  void* v_cache, int32_t* draft, float* logits_opt,
                                  float* layer_dump_opt, int32_t* dev_status, void* ws, size_t ws_bytes,
                                  dflash_trace* trace, dflash_stream_t stream) {
-  return draft_block_impl(c, w, anchor, ctx_len, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+  return draft_block_impl(c, w, anchor, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
                           logits_opt, layer_dump_opt, dev_status, ws, ws_bytes, trace, stream);
+}
+
+dflash_status dflash_draft_block_dyn(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
+                                     const int32_t* ctx_len, const int32_t* gamma_b, int B, int max_ctx_hint,
+                                     void* k_cache, void* v_cache, int32_t* draft, float* logits_opt,
+                                     int32_t* dev_status, void* ws, size_t ws_bytes, dflash_trace* trace,
+                                     dflash_stream_t stream) {
+  if (gamma_b == nullptr) return DFLASH_ERR_INVALID_ARG;
+  return draft_block_impl(c, w, anchor, ctx_len, gamma_b, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+                          logits_opt, nullptr, dev_status, ws, ws_bytes, trace, stream);
 }
 
 dflash_status dflash_draft_block_sample(const dflash_config* c, const dflash_weights* w,
@@ -716,8 +727,8 @@ dflash_status dflash_draft_block_sample(const dflash_config* c, const dflash_wei
                                         int32_t* dev_status, void* ws, size_t ws_bytes,
                                         dflash_trace* trace, dflash_stream_t stream) {
   if (!(temperature > 0.f) || !std::isfinite(temperature) || logits == nullptr) return DFLASH_ERR_INVALID_ARG;
-  return draft_block_impl(c, w, anchor, ctx_len, B, max_ctx_hint, k_cache, v_cache, temperature, seed, draft,
-                          logits, nullptr, dev_status, ws, ws_bytes, trace, stream);
+  return draft_block_impl(c, w, anchor, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, temperature, seed,
+                          draft, logits, nullptr, dev_status, ws, ws_bytes, trace, stream);
 }
 
 dflash_status dflash_verify_sample(const dflash_config* c, const void* target_logits,
@@ -751,8 +762,9 @@ dflash_status dflash_verify_sample(const dflash_config* c, const void* target_lo
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
-dflash_status dflash_verify_accept(const dflash_config* c, const void* target_logits,
-                                   dflash_dtype logits_dtype, const int32_t* draft, int B, int32_t* tau,
+static dflash_status verify_accept_impl(const dflash_config* c, const void* target_logits,
+                                        dflash_dtype logits_dtype, const int32_t* draft,
+                                        const int32_t* gamma_b, int B, int32_t* tau,
                                    int32_t* committed, int32_t* next_anchor, void* ws, size_t ws_bytes,
                                    dflash_trace* trace, dflash_stream_t stream) {
   dflash_status st = dflash_check_config(c);
@@ -770,12 +782,30 @@ dflash_status dflash_verify_accept(const dflash_config* c, const void* target_lo
   const int R = c->gamma + 1;
   const double bytes = static_cast<double>(B) * R * c->vocab * (logits_dtype == DFLASH_BF16 ? 2 : 4);
   tr.before(DFLASH_K_VERIFY, bytes, 0);
-  const cudaError_t e = launch_verify(target_logits, logits_dtype == DFLASH_BF16, draft, B, c->gamma,
+  const cudaError_t e = launch_verify(target_logits, logits_dtype == DFLASH_BF16, draft, gamma_b, B, c->gamma,
                                       c->vocab, tau, committed, next_anchor,
                                       at<unsigned long long>(ws, L.v_keys), at<int>(ws, L.v_count), s,
                                       use_pdl());
   tr.after();
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+dflash_status dflash_verify_accept(const dflash_config* c, const void* target_logits,
+                                   dflash_dtype logits_dtype, const int32_t* draft, int B, int32_t* tau,
+                                   int32_t* committed, int32_t* next_anchor, void* ws, size_t ws_bytes,
+                                   dflash_trace* trace, dflash_stream_t stream) {
+  return verify_accept_impl(c, target_logits, logits_dtype, draft, nullptr, B, tau, committed, next_anchor, ws,
+                            ws_bytes, trace, stream);
+}
+
+dflash_status dflash_verify_accept_dyn(const dflash_config* c, const void* target_logits,
+                                       dflash_dtype logits_dtype, const int32_t* draft, const int32_t* gamma_b,
+                                       int B, int32_t* tau, int32_t* committed, int32_t* next_anchor,
+                                       void* ws, size_t ws_bytes, dflash_trace* trace,
+                                       dflash_stream_t stream) {
+  if (gamma_b == nullptr) return DFLASH_ERR_INVALID_ARG;
+  return verify_accept_impl(c, target_logits, logits_dtype, draft, gamma_b, B, tau, committed, next_anchor, ws,
+                            ws_bytes, trace, stream);
 }
 
 }  // extern "C"

@@ -125,6 +125,8 @@ struct AttnArgs {
   const void* v_cache;
   int layer, n_layers;
   const int* ctx_len;     // [B]
+  const int* gamma_b;     // NULL or [B]: block of sequence b is rows 0..gamma_b[b] (keys
+                          // ctx_len[b] + gamma_b[b] + 1); rows past it are inert
   void* out;              // [B*R, Hq*Dh]
   size_t out_lo_off;      // > 0: bf16 lo = bf16(o - hi) at out + out_lo_off elements
   int* dev_status;
@@ -166,13 +168,17 @@ cudaError_t launch_sample_verify(const void* target, int target_bf16, const floa
                                  const int32_t* draft, int B, int gamma, int V, float temperature,
                                  uint64_t seed, void* ws, int32_t* tau, int32_t* committed,
                                  int32_t* next_anchor, cudaStream_t s, bool pdl);
-cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int32_t* draft,
+// draft[t] = index of keys[t]; with gamma_b, t = b * gamma + j with j >= gamma_b[b] gets -1.
+cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int gamma, const int32_t* gamma_b,
+                                   int32_t* draft,
                                    cudaStream_t s, bool pdl);
 cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
                               int reserve, int* dev_status, cudaStream_t s, bool pdl);
-cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, int B, int gamma,
-                          int V, int32_t* tau, int32_t* committed, int32_t* next_anchor,
-                          unsigned long long* keys, int* counters, cudaStream_t s, bool pdl);
+// Greedy verify-accept; gamma_b NULL or [B] (sequence b verifies its first gamma_b[b] drafts).
+cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, const int32_t* gamma_b,
+                          int B, int gamma, int V, int32_t* tau, int32_t* committed,
+                          int32_t* next_anchor, unsigned long long* keys, int* counters,
+                          cudaStream_t s, bool pdl);
 cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t s, bool pdl);
 
 int num_sms_of_current_device();

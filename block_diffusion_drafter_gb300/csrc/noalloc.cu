@@ -62,7 +62,7 @@ extern "C" dflash_status dflash_verify_accept_noalloc(const dflash_config* c,
   if (cudaMemsetAsync(s->keys, 0, sizeof(unsigned long long) * B * R, cs) != cudaSuccess ||
       cudaMemsetAsync(s->counters, 0, sizeof(int) * B, cs) != cudaSuccess)
     return DFLASH_ERR_CUDA;
-  const cudaError_t e = dfl::launch_verify(target_logits, logits_dtype == DFLASH_BF16, draft, B,
+  const cudaError_t e = dfl::launch_verify(target_logits, logits_dtype == DFLASH_BF16, draft, nullptr, B,
                                            c->gamma, c->vocab, tau, committed, next_anchor, s->keys,
                                            s->counters, cs, dfl::use_pdl());
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;

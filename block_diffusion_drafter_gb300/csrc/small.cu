@@ -137,11 +137,19 @@ __global__ void __launch_bounds__(256) fuse_norm_kernel(const float* u, T* h, co
   }
 }
 
-__global__ void argmax_finalize_kernel(unsigned long long* keys, int n, int32_t* draft) {
+// Block size of sequence b: gamma_b[b] clamped to [1, gamma], or gamma.
+__device__ __forceinline__ int block_gamma(const int32_t* gamma_b, int b, int gamma) {
+  return gamma_b == nullptr ? gamma : min(max(gamma_b[b], 1), gamma);
+}
+
+__global__ void argmax_finalize_kernel(unsigned long long* keys, int n, int gamma, const int32_t* gamma_b,
+                                       int32_t* draft) {
   pdl_launch_dependents();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) draft[i] = static_cast<int32_t>(argmax_key_index(keys[i]));
+  if (i >= n) return;
+  draft[i] = i % gamma < block_gamma(gamma_b, i / gamma, gamma) ? static_cast<int32_t>(argmax_key_index(keys[i]))
+                                                                 : -1;
 }
 
 __global__ void kv_advance_kernel(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
@@ -169,7 +177,8 @@ __global__ void copy_f32_kernel(float* dst, const float* src, size_t n) {
 // integer max (ties -> lowest index); the last CTA of sequence b scans the
 // R argmaxes against the draft and writes tau / committed / next anchor.
 template <typename T>
-__global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int32_t* draft, int gamma,
+__global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int32_t* draft,
+                                                     const int32_t* gamma_b, int gamma,
                                                      int V, int chunk, int32_t* tau,
                                                      int32_t* committed, int32_t* next_anchor,
                                                      unsigned long long* keys, int* counters) {
@@ -217,12 +226,13 @@ __global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int3
   __syncthreads();
   if (!is_last || threadIdx.x != 0) return;
   __threadfence();
+  const int gb = block_gamma(gamma_b, b, gamma);  // this sequence's block size
   int a = 0;
   int32_t t_a = 0;
-  for (int jj = 0; jj <= gamma; ++jj) {
+  for (int jj = 0; jj <= gb; ++jj) {
     const int32_t tj = static_cast<int32_t>(argmax_key_index(__ldcg(&keys[b * R + jj])));
     if (jj == a) {
-      if (jj < gamma && draft[b * gamma + jj] == tj) {
+      if (jj < gb && draft[b * gamma + jj] == tj) {
         committed[b * R + jj] = tj;
         ++a;
       } else {
@@ -265,9 +275,10 @@ cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n
                    row_ss, n_ss, reinterpret_cast<const float*>(gain), D, eps);
 }
 
-cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int32_t* draft, cudaStream_t s,
-                                   bool pdl) {
-  return launch_ex(argmax_finalize_kernel, dim3((n + 127) / 128), dim3(128), 0, s, pdl, keys, n, draft);
+cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int gamma, const int32_t* gamma_b,
+                                   int32_t* draft, cudaStream_t s, bool pdl) {
+  return launch_ex(argmax_finalize_kernel, dim3((n + 127) / 128), dim3(128), 0, s, pdl, keys, n, gamma,
+                   gamma_b, draft);
 }
 
 cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
@@ -287,9 +298,10 @@ int verify_chunks(int B, int R, int V) {
   return c < 1 ? 1 : c;
 }
 
-cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, int B, int gamma, int V,
-                          int32_t* tau, int32_t* committed, int32_t* next_anchor,
-                          unsigned long long* keys, int* counters, cudaStream_t s, bool pdl) {
+cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, const int32_t* gamma_b,
+                          int B, int gamma, int V, int32_t* tau, int32_t* committed,
+                          int32_t* next_anchor, unsigned long long* keys, int* counters,
+                          cudaStream_t s, bool pdl) {
   const int R = gamma + 1;
   const int chunks = verify_chunks(B, R, V);
   int chunk = (V + chunks - 1) / chunks;
@@ -297,11 +309,11 @@ cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, in
   const int n_chunks = (V + chunk - 1) / chunk;
   if (bf16)
     return launch_ex(verify_kernel<__nv_bfloat16>, dim3(n_chunks, R, B), dim3(256), 0, s, pdl,
-                     reinterpret_cast<const __nv_bfloat16*>(logits), draft, gamma, V, chunk, tau,
-                     committed, next_anchor, keys, counters);
+                     reinterpret_cast<const __nv_bfloat16*>(logits), draft, gamma_b, gamma, V, chunk,
+                     tau, committed, next_anchor, keys, counters);
   return launch_ex(verify_kernel<float>, dim3(n_chunks, R, B), dim3(256), 0, s, pdl,
-                   reinterpret_cast<const float*>(logits), draft, gamma, V, chunk, tau, committed,
-                   next_anchor, keys, counters);
+                   reinterpret_cast<const float*>(logits), draft, gamma_b, gamma, V, chunk, tau,
+                   committed, next_anchor, keys, counters);
 }
 
 int num_sms_of_current_device() {

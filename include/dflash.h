@@ -220,6 +220,37 @@ dflash_status dflash_draft_block(const dflash_config* cfg, const dflash_weights*
                                  void* ws, size_t ws_bytes, dflash_trace* trace,
                                  dflash_stream_t stream);
 
+/* Drafting pass with a block size per sequence (SURVEY's NEXT row "dynamic
+ * gamma"; [P1] block-size ablation: a drafter trained with block 16 serves
+ * smaller inference blocks, which makes per-request block sizes possible;
+ * the scheduling policy itself is left to the caller). Sequence b drafts
+ * the block [anchor_b, m x gamma_b[b]] at positions ctx_len[b] + 0..gamma_b[b]:
+ * exactly dflash_draft_block with gamma = gamma_b[b] for that sequence. Rows
+ * past a sequence's block are computed on the padded layout but are neither
+ * keys nor drafts: draft[b, j] = -1 for j >= gamma_b[b].
+ * gamma_b: device [B] int32, values clamped to [1, cfg.gamma].
+ * logits_opt rows j >= gamma_b[b] hold unused values. Other arguments as in
+ * dflash_draft_block (no layer dump). */
+dflash_status dflash_draft_block_dyn(const dflash_config* cfg, const dflash_weights* w,
+                                     const int32_t* anchor, const int32_t* ctx_len,
+                                     const int32_t* gamma_b, int B, int max_ctx_hint,
+                                     void* k_cache, void* v_cache, int32_t* draft,
+                                     float* logits_opt, int32_t* dev_status, void* ws,
+                                     size_t ws_bytes, dflash_trace* trace,
+                                     dflash_stream_t stream);
+
+/* Greedy verification of blocks of per-sequence size gamma_b[b] (clamped to
+ * [1, cfg.gamma]): dflash_verify_accept with gamma = gamma_b[b], reading
+ * target rows 0..gamma_b[b] of the [B, gamma+1, V] layout and drafts
+ * 0..gamma_b[b]-1 of the [B, gamma] layout; tau[b] in [1, gamma_b[b] + 1];
+ * committed[b] is padded with -1 to gamma + 1 entries. */
+dflash_status dflash_verify_accept_dyn(const dflash_config* cfg, const void* target_logits,
+                                       dflash_dtype logits_dtype, const int32_t* draft,
+                                       const int32_t* gamma_b, int B, int32_t* tau,
+                                       int32_t* committed, int32_t* next_anchor, void* ws,
+                                       size_t ws_bytes, dflash_trace* trace,
+                                       dflash_stream_t stream);
+
 /* Sampling mode of the drafting pass (temperature > 0): the pass of
  * dflash_draft_block, except that draft token j of sequence b is a draw from
  * softmax(logits_j / temperature) (the temperature-1 setting of [P1] result

@@ -142,3 +142,14 @@ def test_sampling_entry_points_reject_bad_arguments_before_any_launch(lib):
     # workspace too small
     assert L.dflash_verify_sample(ctypes.byref(cfg), fake, lib.F32, fake, fake, 1, 1.0, 1, fake, fake, fake,
                                   fake, 16, None, None) == lib.ERR_WORKSPACE
+
+
+def test_per_sequence_gamma_calls_require_the_gamma_array(lib):
+    L = lib.load()
+    cfg = lib.config_from_workload(synth.WORKLOADS["tiny_f32_L1_N128"])
+    w = lib.WeightsStruct()
+    fake = 256
+    assert L.dflash_draft_block_dyn(ctypes.byref(cfg), ctypes.byref(w), fake, fake, None, 1, 0, fake, fake, fake,
+                                    None, fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_verify_accept_dyn(ctypes.byref(cfg), fake, lib.F32, fake, None, 1, fake, fake, fake, fake,
+                                      1 << 30, None, None) == lib.ERR_INVALID_ARG
