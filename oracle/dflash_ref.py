@@ -163,7 +163,7 @@ def attention(cfg: Cfg, q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarr
 # -- a3..a8: one-pass block drafting ------------------------------------------
 
 def draft_block(cfg: Cfg, W: dict, anchor: int, k_ctx, v_ctx, n_ctx: int,
-                want_dumps: bool = False) -> dict:
+                want_dumps: bool = False, ids=None) -> dict:
     """One drafting pass for one sequence, [P4] §3.3 and §3.2, [P1] "추론 구조":
 
       input ids  [anchor, m, ..., m] (R = gamma + 1 rows), positions
@@ -181,11 +181,14 @@ def draft_block(cfg: Cfg, W: dict, anchor: int, k_ctx, v_ctx, n_ctx: int,
 
     W: stacked weights (arrays or CPU tensors, any float dtype).
     k_ctx, v_ctx: per layer [Hkv, >= n_ctx, Dh] injected entries.
+    ids: optional block input [R] (row 0 the anchor) replacing [anchor, m, ..., m]
+    -- the partially unmasked block of multi-step drafting.
     Returns dict(logits [gamma, V], draft [gamma], dumps [L+1, R, D] or None)."""
     L, R, D = cfg.n_layers, cfg.rows, cfg.d_model
     Hq, Hkv, Dh, F = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.d_ffn
     eps = cfg.rms_eps
-    ids = np.array([anchor] + [cfg.mask_token_id] * cfg.gamma)
+    ids = np.array([anchor] + [cfg.mask_token_id] * cfg.gamma) if ids is None else np.asarray(ids)
+    assert ids.shape == (R,) and ids[0] == anchor
     pos = n_ctx + np.arange(R)
     h = f64(W["embed"][ids])
     dumps = [h.copy()] if want_dumps else None
@@ -349,3 +352,54 @@ def verify_sample(target_logits, draft_logits, draft, T: float, seed: int, b: in
     committed[:a] = d[:a]
     committed[a] = y
     return a + 1, committed, int(y)
+
+
+# -- NEXT: multi-step confidence unmasking within a block --------------------
+#
+# [P2] "블록 확산 디코딩" drafting paragraph: the block starts as [MASK] at
+# every position; each pass predicts all masked positions at once
+# (bidirectional attention inside the block); the positions predicted with
+# the highest confidence are unmasked first (their [MASK] replaced by the
+# predicted token), and the passes repeat until the whole block is filled;
+# the target then verifies the block at once. The pages give no schedule.
+# Readings: confidence = max_v softmax(logits_j); S passes; pass s (0-based)
+# unmasks ceil(m / (S - s)) of the m positions still masked; ties of
+# confidence go to the lower position; an unmasked position keeps its token
+# as input to later passes.
+
+
+def confidence(logits) -> np.ndarray:
+    """max_v softmax(logits_j): 1 / sum_v exp(l_v - max_v l)."""
+    lg = f64(logits)
+    return 1.0 / np.exp(lg - lg.max(axis=-1, keepdims=True)).sum(axis=-1)
+
+
+def unmask_step(ids, logits, steps_left: int, mask_id: int):
+    """One unmasking decision for one block. ids [R] (row 0 the anchor),
+    logits [gamma, V] of the pass on ids. Returns the new ids [R]."""
+    ids = np.array(ids, dtype=np.int64)
+    masked = [j for j in range(ids.shape[0] - 1) if ids[j + 1] == mask_id]
+    if not masked:
+        return ids
+    k = -(-len(masked) // steps_left)              # ceil(m / steps_left)
+    conf = confidence(logits)
+    order = sorted(masked, key=lambda j: (-conf[j], j))
+    tok = argmax_lowest(f64(logits))
+    for j in order[:k]:
+        ids[j + 1] = tok[j]
+    return ids
+
+
+def draft_block_iterative(cfg: Cfg, W: dict, anchor: int, k_ctx, v_ctx, n_ctx: int,
+                          n_steps: int) -> dict:
+    """Multi-step drafting of one block: n_steps passes of draft_block, each
+    followed by unmask_step. Returns dict(draft [gamma], ids per step
+    [n_steps + 1, R], logits per step [n_steps, gamma, V])."""
+    ids = np.array([anchor] + [cfg.mask_token_id] * cfg.gamma, dtype=np.int64)
+    hist, lgs = [ids.copy()], []
+    for s in range(n_steps):
+        out = draft_block(cfg, W, anchor, k_ctx, v_ctx, n_ctx, ids=ids)
+        lgs.append(out["logits"])
+        ids = unmask_step(ids, out["logits"], n_steps - s, cfg.mask_token_id)
+        hist.append(ids.copy())
+    return {"draft": ids[1:], "ids": np.stack(hist), "logits": np.stack(lgs)}
