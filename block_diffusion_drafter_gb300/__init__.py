@@ -76,6 +76,12 @@ _SIGS = {
                                     _I, _I, _P, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
     "dflash_verify_accept_dyn": (_I, [ctypes.POINTER(Config), _P, _I, _P, _P, _I, _P, _P, _P, _P, _SZ,
                                       ctypes.POINTER(Trace), _P]),
+    "dflash_draft_block_ids": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _I, _I,
+                                    _P, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
+    "dflash_unmask_step": (_I, [ctypes.POINTER(Config), _P, _P, _P, _I, _I, _P, _SZ, ctypes.POINTER(Trace),
+                                _P]),
+    "dflash_draft_block_iter": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _I, _I,
+                                     _P, _P, _I, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
     "dflash_draft_block_sample": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P,
                                        _I, _I, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P,
                                        _P, _SZ, ctypes.POINTER(Trace), _P]),
@@ -273,6 +279,32 @@ def dflash_verify_accept_dyn(cfg, target_logits, draft, gamma_b, tau, committed,
         ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), _ptr(gamma_b), B, _ptr(tau),
         _ptr(committed), _ptr(next_anchor), ws.ptr, ws.nbytes,
         ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_draft_block_ids(cfg, w: Weights, ids, ctx_len, max_ctx_hint, k_cache, v_cache, draft, dev_status,
+                           ws: Workspace, logits=None, trace=None, stream=None):
+    """Drafting pass on explicit block inputs ids [B, R]."""
+    B = ids.shape[0]
+    _check("dflash_draft_block_ids", load().dflash_draft_block_ids(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(ids), _ptr(ctx_len), B, int(max_ctx_hint),
+        _ptr(k_cache), _ptr(v_cache), _ptr(draft), _ptr(logits), _ptr(dev_status), ws.ptr, ws.nbytes,
+        ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_unmask_step(cfg, logits, draft, ids, steps_left, ws: Workspace, trace=None, stream=None):
+    _check("dflash_unmask_step", load().dflash_unmask_step(
+        ctypes.byref(cfg), _ptr(logits), _ptr(draft), _ptr(ids), ids.shape[0], int(steps_left), ws.ptr,
+        ws.nbytes, ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_draft_block_iter(cfg, w: Weights, anchor, ctx_len, max_ctx_hint, k_cache, v_cache, n_steps, ids,
+                            draft, logits, dev_status, ws: Workspace, trace=None, stream=None):
+    """n_steps passes of multi-step confidence unmasking."""
+    B = anchor.shape[0]
+    _check("dflash_draft_block_iter", load().dflash_draft_block_iter(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(anchor), _ptr(ctx_len), B, int(max_ctx_hint),
+        _ptr(k_cache), _ptr(v_cache), int(n_steps), _ptr(ids), _ptr(draft), _ptr(logits), _ptr(dev_status),
+        ws.ptr, ws.nbytes, ctypes.byref(trace) if trace is not None else None, _stream(stream)))
 
 
 def dflash_draft_block_sample(cfg, w: Weights, anchor, ctx_len, max_ctx_hint, k_cache, v_cache,

@@ -467,7 +467,7 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
 extern "C" {
 
 static dflash_status draft_block_impl(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
-                                      const int32_t* ctx_len, const int32_t* gamma_b, int B,
+                                      const int32_t* ids, const int32_t* ctx_len, const int32_t* gamma_b, int B,
                                       int max_ctx_hint, void* k_cache,
                                       void* v_cache, float temperature, uint64_t seed, int32_t* draft,
                                       float* logits_opt, float* layer_dump_opt, int32_t* dev_status, void* ws,
@@ -475,7 +475,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
   if (w == nullptr || B < 1 || B > c->max_batch || max_ctx_hint < 0) return DFLASH_ERR_INVALID_ARG;
-  if (anchor == nullptr || ctx_len == nullptr || k_cache == nullptr || v_cache == nullptr ||
+  if ((anchor == nullptr && ids == nullptr) || ctx_len == nullptr || k_cache == nullptr || v_cache == nullptr ||
       draft == nullptr || dev_status == nullptr || w->embed == nullptr || w->g_final == nullptr ||
       w->lm_head == nullptr || w->g_attn == nullptr || w->w_qkv == nullptr || w->w_o == nullptr ||
       w->g_ffn == nullptr || w->w_gateup == nullptr || w->w_down == nullptr || !rope_ok(c, w))
@@ -576,7 +576,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
   };
 
   cx.tr.before(DFLASH_K_NORM, row_bytes + static_cast<double>(rows) * D * es, 0);
-  st = fail(launch_embed(w->embed, anchor, c->mask_token_id, B, R, D, V, bf16, h, gain_of(w->g_attn, 0),
+  st = fail(launch_embed(w->embed, anchor, ids, c->mask_token_id, B, R, D, V, bf16, h, gain_of(w->g_attn, 0),
                          xn, xn_lo, ss, keys, nmask, dev_status, cx.s, cx.pdl));
   cx.tr.after();
   if (st != DFLASH_OK) return st;
@@ -706,7 +706,7 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
                                  void* v_cache, int32_t* draft, float* logits_opt,
                                  float* layer_dump_opt, int32_t* dev_status, void* ws, size_t ws_bytes,
                                  dflash_trace* trace, dflash_stream_t stream) {
-  return draft_block_impl(c, w, anchor, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+  return draft_block_impl(c, w, anchor, nullptr, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
                           logits_opt, layer_dump_opt, dev_status, ws, ws_bytes, trace, stream);
 }
 
@@ -716,8 +716,61 @@ dflash_status dflash_draft_block_dyn(const dflash_config* c, const dflash_weight
                                      int32_t* dev_status, void* ws, size_t ws_bytes, dflash_trace* trace,
                                      dflash_stream_t stream) {
   if (gamma_b == nullptr) return DFLASH_ERR_INVALID_ARG;
-  return draft_block_impl(c, w, anchor, ctx_len, gamma_b, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+  return draft_block_impl(c, w, anchor, nullptr, ctx_len, gamma_b, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
                           logits_opt, nullptr, dev_status, ws, ws_bytes, trace, stream);
+}
+
+dflash_status dflash_draft_block_ids(const dflash_config* c, const dflash_weights* w, const int32_t* ids,
+                                     const int32_t* ctx_len, int B, int max_ctx_hint, void* k_cache,
+                                     void* v_cache, int32_t* draft, float* logits_opt, int32_t* dev_status,
+                                     void* ws, size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
+  if (ids == nullptr) return DFLASH_ERR_INVALID_ARG;
+  return draft_block_impl(c, w, nullptr, ids, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+                          logits_opt, nullptr, dev_status, ws, ws_bytes, trace, stream);
+}
+
+dflash_status dflash_unmask_step(const dflash_config* c, const float* logits, const int32_t* draft, int32_t* ids,
+                                 int B, int steps_left, void* ws, size_t ws_bytes, dflash_trace* trace,
+                                 dflash_stream_t stream) {
+  dflash_status st = dflash_check_config(c);
+  if (st != DFLASH_OK) return st;
+  if (logits == nullptr || draft == nullptr || ids == nullptr || B < 1 || B > c->max_batch || steps_left < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!trace_ok(trace)) return DFLASH_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c);
+  if (ws == nullptr || ws_bytes < L.fixed) return DFLASH_ERR_WORKSPACE;
+  if ((st = check_arch()) != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Tracer tr{trace, s};
+  tr.before(DFLASH_K_VERIFY, static_cast<double>(B) * c->gamma * c->vocab * 4, 0);
+  const cudaError_t e = launch_unmask_step(logits, draft, B, c->gamma, c->vocab, c->mask_token_id, steps_left,
+                                           at<void>(ws, L.samp), ids, s, use_pdl());
+  tr.after();
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+dflash_status dflash_draft_block_iter(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
+                                      const int32_t* ctx_len, int B, int max_ctx_hint, void* k_cache,
+                                      void* v_cache, int n_steps, int32_t* ids, int32_t* draft, float* logits,
+                                      int32_t* dev_status, void* ws, size_t ws_bytes, dflash_trace* trace,
+                                      dflash_stream_t stream) {
+  dflash_status st = dflash_check_config(c);
+  if (st != DFLASH_OK) return st;
+  if (anchor == nullptr || ids == nullptr || draft == nullptr || logits == nullptr || B < 1 ||
+      B > c->max_batch || n_steps < 1 || n_steps > c->gamma)
+    return DFLASH_ERR_INVALID_ARG;
+  if ((st = check_arch()) != DFLASH_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_ids_init(anchor, c->mask_token_id, B, c->gamma + 1, ids, s, use_pdl()) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  for (int step = 0; step < n_steps; ++step) {
+    st = draft_block_impl(c, w, nullptr, ids, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
+                          logits, nullptr, dev_status, ws, ws_bytes, trace, stream);
+    if (st != DFLASH_OK) return st;
+    st = dflash_unmask_step(c, logits, draft, ids, B, n_steps - step, ws, ws_bytes, trace, stream);
+    if (st != DFLASH_OK) return st;
+  }
+  return launch_ids_to_draft(ids, B, c->gamma, draft, s, use_pdl()) == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
 dflash_status dflash_draft_block_sample(const dflash_config* c, const dflash_weights* w,
@@ -727,7 +780,7 @@ dflash_status dflash_draft_block_sample(const dflash_config* c, const dflash_wei
                                         int32_t* dev_status, void* ws, size_t ws_bytes,
                                         dflash_trace* trace, dflash_stream_t stream) {
   if (!(temperature > 0.f) || !std::isfinite(temperature) || logits == nullptr) return DFLASH_ERR_INVALID_ARG;
-  return draft_block_impl(c, w, anchor, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, temperature, seed,
+  return draft_block_impl(c, w, anchor, nullptr, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, temperature, seed,
                           draft, logits, nullptr, dev_status, ws, ws_bytes, trace, stream);
 }
 

@@ -142,16 +142,30 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl);
 
 // Small row kernels.
-// h[b*R + i] = embed[id] (id = anchor[b] for i == 0, else mask_id), fp32; also
-// xg = gain (.) h in cfg dtype and ss[row][c] = sum of h^2 over features
-// 128c..128c+127 (the first layer's folded RMSNorm); zeroes keys[0..n_keys).
-cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
+// h[b*R + i] = embed[id] (id = ids[b*R + i] when ids is given, else anchor[b]
+// for i == 0 and mask_id otherwise), fp32; also xg = gain (.) h in cfg dtype
+// and ss[row][c] = sum of h^2 over features 128c..128c+127 (the first
+// layer's folded RMSNorm); zeroes keys[0..n_keys).
+cudaError_t launch_embed(const void* embed, const int* anchor, const int* ids, int mask_id, int B, int R,
+                         int D, int V,
                          int bf16, float* h, const void* gain, void* xg, size_t xg_lo_off, float* ss,
                          unsigned long long* keys, int n_keys, int* dev_status, cudaStream_t s,
                          bool pdl);
 // h[t] = gain * u[t] / sqrt(sum(row_ss[t]) / D + eps), u fp32, h in cfg dtype.
 cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
                              int T, int D, float eps, int bf16, cudaStream_t s, bool pdl);
+// Multi-step confidence unmasking (unmask.cu). ids [B, R] block inputs.
+cudaError_t launch_ids_init(const int32_t* anchor, int mask_id, int B, int R, int32_t* ids, cudaStream_t s,
+                            bool pdl);
+// One unmasking decision per sequence from the pass's logits [B, gamma, V]
+// (fp32) and argmax tokens draft [B, gamma]: the ceil(m / steps_left) most
+// confident still-masked positions take their token. ws: sample_ws_bytes.
+cudaError_t launch_unmask_step(const float* logits, const int32_t* draft, int B, int gamma, int V,
+                               int mask_id, int steps_left, void* ws, int32_t* ids, cudaStream_t s,
+                               bool pdl);
+cudaError_t launch_ids_to_draft(const int32_t* ids, int B, int gamma, int32_t* draft, cudaStream_t s,
+                                bool pdl);
+
 // Sampling verification (temperature > 0): rejection-acceptance over the
 // target logits [B, gamma+1, V] (bf16 or fp32) and the drafter logits
 // [B, gamma, V] (fp32) of the sampled drafts. Three launches: per-chunk

@@ -64,15 +64,16 @@ __device__ __forceinline__ float4 sub_hi4<__nv_bfloat16>(float4 x) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* anchor, int mask_id,
-                                                    int R, int D, int V, float* h, const T* gain,
+__global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* anchor, const int* ids,
+                                                    int mask_id, int R, int D, int V, float* h, const T* gain,
                                                     T* xg, size_t xg_lo_off, float* ss,
                                                     unsigned long long* keys, int n_keys,
                                                     int* dev_status) {
   pdl_launch_dependents();
   pdl_wait();
   const int r = blockIdx.x, b = r / R, i = r % R;
-  int id = i == 0 ? anchor[b] : mask_id;
+  // explicit block ids (multi-step drafting), else [anchor, m, ..., m]
+  int id = ids != nullptr ? ids[r] : (i == 0 ? anchor[b] : mask_id);
   if (id < 0 || id >= V) {
     if (threadIdx.x == 0) report(dev_status, DFLASH_ERR_INVALID_ARG);
     id = 0;
@@ -250,17 +251,18 @@ __global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int3
 
 }  // namespace
 
-cudaError_t launch_embed(const void* embed, const int* anchor, int mask_id, int B, int R, int D, int V,
+cudaError_t launch_embed(const void* embed, const int* anchor, const int* ids, int mask_id, int B, int R,
+                         int D, int V,
                          int bf16, float* h, const void* gain, void* xg, size_t xg_lo_off, float* ss,
                          unsigned long long* keys, int n_keys, int* dev_status, cudaStream_t s,
                          bool pdl) {
   if (bf16)
     return launch_ex(embed_kernel<__nv_bfloat16>, dim3(B * R), dim3(256), 0, s, pdl,
-                     reinterpret_cast<const __nv_bfloat16*>(embed), anchor, mask_id, R, D, V, h,
+                     reinterpret_cast<const __nv_bfloat16*>(embed), anchor, ids, mask_id, R, D, V, h,
                      reinterpret_cast<const __nv_bfloat16*>(gain), reinterpret_cast<__nv_bfloat16*>(xg),
                      xg_lo_off, ss, keys, n_keys, dev_status);
   return launch_ex(embed_kernel<float>, dim3(B * R), dim3(256), 0, s, pdl,
-                   reinterpret_cast<const float*>(embed), anchor, mask_id, R, D, V, h,
+                   reinterpret_cast<const float*>(embed), anchor, ids, mask_id, R, D, V, h,
                    reinterpret_cast<const float*>(gain), reinterpret_cast<float*>(xg), size_t(0), ss,
                    keys, n_keys, dev_status);
 }

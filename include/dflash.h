@@ -251,6 +251,40 @@ dflash_status dflash_verify_accept_dyn(const dflash_config* cfg, const void* tar
                                        size_t ws_bytes, dflash_trace* trace,
                                        dflash_stream_t stream);
 
+/* Multi-step confidence unmasking ([P2] drafting paragraph: the block
+ * starts as [MASK] everywhere; each pass predicts all masked positions; the
+ * most confident positions are unmasked first; the passes repeat until the
+ * block is full). Readings: confidence = max_v softmax(logits_j); pass s of
+ * n_steps fills ceil(m / (n_steps - s)) of the m still-masked positions with
+ * their argmax tokens, ties to the lower position; filled positions are
+ * inputs to later passes.
+ *
+ * dflash_draft_block_ids: the drafting pass on explicit block inputs
+ *   ids [B, R] (device int32; row 0 the anchor, mask_token_id where masked)
+ *   instead of [anchor, m, ..., m]; draft = argmax of every mask row's logits.
+ * dflash_unmask_step: one decision: logits [B, gamma, V] fp32 and draft
+ *   [B, gamma] of the pass on ids; fills the ceil(m / steps_left) most
+ *   confident masked positions of ids (in place). steps_left >= 1.
+ * dflash_draft_block_iter: n_steps (1..gamma) passes and decisions from
+ *   [anchor, m, ..., m]; ids [B, R] receives the final block, draft [B, gamma]
+ *   its tokens; logits [B, gamma, V] fp32 is required scratch (it holds the
+ *   last pass's logits). n_steps = 1 is dflash_draft_block's draft. */
+dflash_status dflash_draft_block_ids(const dflash_config* cfg, const dflash_weights* w,
+                                     const int32_t* ids, const int32_t* ctx_len, int B,
+                                     int max_ctx_hint, void* k_cache, void* v_cache, int32_t* draft,
+                                     float* logits_opt, int32_t* dev_status, void* ws,
+                                     size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream);
+dflash_status dflash_unmask_step(const dflash_config* cfg, const float* logits,
+                                 const int32_t* draft, int32_t* ids, int B, int steps_left,
+                                 void* ws, size_t ws_bytes, dflash_trace* trace,
+                                 dflash_stream_t stream);
+dflash_status dflash_draft_block_iter(const dflash_config* cfg, const dflash_weights* w,
+                                      const int32_t* anchor, const int32_t* ctx_len, int B,
+                                      int max_ctx_hint, void* k_cache, void* v_cache, int n_steps,
+                                      int32_t* ids, int32_t* draft, float* logits,
+                                      int32_t* dev_status, void* ws, size_t ws_bytes,
+                                      dflash_trace* trace, dflash_stream_t stream);
+
 /* Sampling mode of the drafting pass (temperature > 0): the pass of
  * dflash_draft_block, except that draft token j of sequence b is a draw from
  * softmax(logits_j / temperature) (the temperature-1 setting of [P1] result

@@ -153,3 +153,21 @@ def test_per_sequence_gamma_calls_require_the_gamma_array(lib):
                                     None, fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
     assert L.dflash_verify_accept_dyn(ctypes.byref(cfg), fake, lib.F32, fake, None, 1, fake, fake, fake, fake,
                                       1 << 30, None, None) == lib.ERR_INVALID_ARG
+
+
+def test_unmasking_calls_reject_bad_arguments(lib):
+    L = lib.load()
+    cfg = lib.config_from_workload(synth.WORKLOADS["tiny_f32_L1_N128"])
+    w = lib.WeightsStruct()
+    fake = 256
+    assert L.dflash_unmask_step(ctypes.byref(cfg), fake, fake, fake, 1, 0, fake, 1 << 30, None,
+                                None) == lib.ERR_INVALID_ARG          # steps_left >= 1
+    assert L.dflash_unmask_step(ctypes.byref(cfg), None, fake, fake, 1, 1, fake, 1 << 30, None,
+                                None) == lib.ERR_INVALID_ARG
+    assert L.dflash_unmask_step(ctypes.byref(cfg), fake, fake, fake, 1, 1, fake, 16, None,
+                                None) == lib.ERR_WORKSPACE
+    for n in (0, cfg.gamma + 1):                                      # 1 <= n_steps <= gamma
+        assert L.dflash_draft_block_iter(ctypes.byref(cfg), ctypes.byref(w), fake, fake, 1, 0, fake, fake, n,
+                                         fake, fake, fake, fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+    assert L.dflash_draft_block_ids(ctypes.byref(cfg), ctypes.byref(w), None, fake, 1, 0, fake, fake, fake, None,
+                                    fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
