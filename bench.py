@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     p.add_argument("--cpu-steps", type=int, default=2, help="oracle steps timed for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-next-rows", action="store_true",
+                   help="skip the timing of the drafting variants (sampling, per-sequence gamma, unmasking)")
     return p.parse_args()
 
 
@@ -154,14 +156,19 @@ class DraftCycle:
         self.max_ctx = int(synth.ctx_lengths(wl).max())
         torch.cuda.synchronize()
 
-    def step_draft(self, trace=None):
-        """Fusion and injection of the step's new rows, then the drafting pass."""
+    def step_inject(self, trace=None):
+        """Fusion and injection of the step's new rows."""
         d, wl = self.dfl, self.wl
         self.ctx_len.copy_(self.ctx0)
         d.dflash_ctx_fuse(self.cfg, self.w, self.step_taps, self.h_new.view(-1, wl.d_model), self.ws,
                           trace=trace)
         d.dflash_kv_inject(self.cfg, self.w, self.h_new, self.n_new, self.ctx_len, self.k_cache,
                            self.v_cache, self.status, self.ws, trace=trace)
+
+    def step_draft(self, trace=None):
+        """Fusion and injection of the step's new rows, then the drafting pass."""
+        d = self.dfl
+        self.step_inject(trace)
         d.dflash_draft_block(self.cfg, self.w, self.anchor, self.ctx_len, self.max_ctx, self.k_cache,
                              self.v_cache, self.draft, self.status, self.ws, trace=trace)
 
@@ -171,6 +178,45 @@ class DraftCycle:
 
     def step(self, trace=None):
         self.step_draft(trace)
+        self.step_verify(trace)
+
+    # the cycle with the drafting variants built beyond the greedy one-pass draft
+    def _variant_buffers(self):
+        if not hasattr(self, "v_logits"):
+            B, wl = self.wl.batch, self.wl
+            self.v_logits = torch.empty((B, wl.gamma, wl.vocab), dtype=torch.float32, device=self.dev)
+            self.v_ids = torch.empty((B, wl.rows), dtype=torch.int32, device=self.dev)
+            self.v_gamma = torch.full((B,), wl.gamma // 2, dtype=torch.int32, device=self.dev)
+
+    def step_sample(self, trace=None, temperature=1.0, seed=12345):
+        """Sampled drafts (temperature T) and rejection-acceptance verification."""
+        d = self.dfl
+        self._variant_buffers()
+        self.step_inject(trace)
+        d.dflash_draft_block_sample(self.cfg, self.w, self.anchor, self.ctx_len, self.max_ctx, self.k_cache,
+                                    self.v_cache, temperature, seed, self.draft, self.v_logits, self.status,
+                                    self.ws, trace=trace)
+        d.dflash_verify_sample(self.cfg, self.target, self.v_logits, self.draft, temperature, seed, self.tau,
+                               self.committed, self.next_anchor, self.ws, trace=trace)
+
+    def step_dyn(self, trace=None):
+        """Per-sequence block size gamma/2 (drafting and verification)."""
+        d = self.dfl
+        self._variant_buffers()
+        self.step_inject(trace)
+        d.dflash_draft_block_dyn(self.cfg, self.w, self.anchor, self.ctx_len, self.v_gamma, self.max_ctx,
+                                 self.k_cache, self.v_cache, self.draft, self.status, self.ws, trace=trace)
+        d.dflash_verify_accept_dyn(self.cfg, self.target, self.draft, self.v_gamma, self.tau, self.committed,
+                                   self.next_anchor, self.ws, trace=trace)
+
+    def step_unmask(self, trace=None, n_steps=4):
+        """Multi-step confidence unmasking (n_steps passes), greedy verification."""
+        d = self.dfl
+        self._variant_buffers()
+        self.step_inject(trace)
+        d.dflash_draft_block_iter(self.cfg, self.w, self.anchor, self.ctx_len, self.max_ctx, self.k_cache,
+                                  self.v_cache, n_steps, self.v_ids, self.draft, self.v_logits, self.status,
+                                  self.ws, trace=trace)
         self.step_verify(trace)
 
     def launches_per_step(self) -> int:
@@ -190,6 +236,35 @@ def time_steps(fn, steps: int, stream) -> float:
     end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end)
+
+
+def measure_variant(cyc: DraftCycle, fn, steps: int, tokens: int, peak_gbs: float) -> dict:
+    """One drafting-variant cycle (fusion + injection + its drafting and
+    verification) replayed as a graph: us per step, drafted tokens/s, and its
+    algorithmic bytes (from one traced run) against the measured HBM peak."""
+    fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(3):
+        g.replay()
+    ms = time_steps(g.replay, steps, torch.cuda.current_stream())
+    rec = cyc.dfl.TraceRecorder(4096)
+    rec.reset()
+    fn(trace=rec.struct)
+    torch.cuda.synchronize()
+    b = sum(r[1] for r in rec.records())
+    us = 1000.0 * ms / steps
+    gbs = b / (us * 1e-6) / 1e9
+    return {"us_per_step": round(us, 2), "drafted_tok_s": round(tokens / (us * 1e-6), 1),
+            "algorithmic_gb_per_step": round(b / 1e9, 3), "achieved_gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / peak_gbs, 4), "steps": steps}
 
 
 def kernel_roofline(cyc: DraftCycle, peak_gbs: float, reps: int = 5):
@@ -418,6 +493,18 @@ def run_gpu(args):
             "unit": "GB/s", "frac": round(g.get("frac_of_hbm", 0.0), 4),
             "traffic": traffic, "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
     step_bytes = sum(v["bytes_per_launch"] * v["launches_per_step"] for v in kern.values())
+    next_rows = None
+    if rank == 0 and not args.no_next_rows:
+        B, gam = wl.batch, wl.gamma
+        next_rows = {
+            "sampling_T1": dict(measure_variant(cyc, cyc.step_sample, min(args.steps, 50), B * gam, hbm),
+                                what="sampled drafts at T=1 + rejection-acceptance verification"),
+            "per_sequence_gamma_half": dict(measure_variant(cyc, cyc.step_dyn, min(args.steps, 50),
+                                                            B * (gam // 2), hbm),
+                                            what=f"block size {gam // 2} of {gam} per sequence"),
+            "unmask_4_passes": dict(measure_variant(cyc, cyc.step_unmask, min(args.steps, 20), B * gam, hbm),
+                                    what="multi-step confidence unmasking, 4 passes"),
+        }
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
@@ -446,6 +533,7 @@ def run_gpu(args):
             "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         for k, v in kern.items()},
             "cpu_baseline": cpu,
+            "next_rows": next_rows,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
