@@ -12,9 +12,9 @@
 // Three launches over one workspace region:
 //   1. sample_stats_kernel: grid (V chunks, B x (2 gamma + 1) rows): per row
 //      and chunk the max m of logit / T and sum exp(logit / T - m);
-//   2. sample_decide_kernel: one CTA per sequence combines each row's chunks
-//      in ascending order and scans the acceptance test;
-//   3. sample_resid_kernel: grid (V chunks, B): per chunk the best packed
+//   2. sample_decide_kernel: one CTA per sequence merges each row's chunks
+//      (a warp per row, fixed tree) and scans the acceptance test;
+//   3. sample_resid_kernel: grid (512-entry V chunks, B): per chunk the best packed
 //      (score, index) key of the residual and of the plain p_a / p_gamma
 //      draw, atomicMax per sequence; the last CTA of a sequence decides.
 #include <cuda_bf16.h>
@@ -28,6 +28,9 @@ namespace {
 
 constexpr int kStatThreads = 256;
 constexpr int kPerThread = kSampChunk / kStatThreads;
+constexpr int kMaxGammaSample = 32;  // block rows the decision kernel holds (gamma <= 16)
+constexpr int kResidChunk = 512;     // vocabulary entries per residual-draw CTA
+constexpr int kResidPer = kResidChunk / kStatThreads;
 
 template <typename T>
 __device__ __forceinline__ float logit_at(const T* p, size_t i);
@@ -86,7 +89,7 @@ __device__ __forceinline__ unsigned long long block_keymax256(unsigned long long
 // Row r of sequence b: r <= gamma a target row, r > gamma draft row r - gamma - 1.
 template <typename TT>
 __global__ void __launch_bounds__(kStatThreads)
-    sample_stats_kernel(const TT* target, const float* draft_logits, int gamma, int V, float temp,
+    sample_stats_kernel(const TT* target, const float* draft_logits, int gamma, int V, float inv_t,
                         int n_chunks, float2* partials) {
   __shared__ float red[8];
   pdl_launch_dependents();
@@ -102,7 +105,7 @@ __global__ void __launch_bounds__(kStatThreads)
     x[i] = -INFINITY;
     if (v < V)
       x[i] = (r < R ? logit_at(target, (static_cast<size_t>(b) * R + r) * V + v)
-                    : draft_logits[(static_cast<size_t>(b) * gamma + (r - R)) * V + v]) / temp;
+                    : draft_logits[(static_cast<size_t>(b) * gamma + (r - R)) * V + v]) * inv_t;
     m = fmaxf(m, x[i]);
   }
   m = block_max256(m, red);
@@ -116,38 +119,59 @@ __global__ void __launch_bounds__(kStatThreads)
   if (threadIdx.x == 0) partials[static_cast<size_t>(row) * n_chunks + c] = make_float2(m, s);
 }
 
+// (m, s) pairs of max and sum exp(x - m): the pair of the union.
+__device__ __forceinline__ void softmax_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) { m = m2; s = s2; return; }
+  const float nm = fmaxf(m, m2);
+  s = s * expf(m - nm) + s2 * expf(m2 - nm);
+  m = nm;
+}
+
+// One CTA per sequence: a warp per row merges the row's chunk statistics
+// (lane-strided, then a fixed shuffle tree); the gamma candidates' p and q
+// and uniforms are computed in parallel; one thread scans the acceptance
+// test over shared memory.
 template <typename TT>
-__global__ void __launch_bounds__(64)
+__global__ void __launch_bounds__(1024)
     sample_decide_kernel(const TT* target, const float* draft_logits, const int32_t* draft, int gamma,
-                         int V, float temp, uint64_t seed, int n_chunks, const float2* partials,
+                         int V, float inv_t, uint64_t seed, int n_chunks, const float2* partials,
                          SampleState* state, unsigned long long* keys, unsigned int* counters) {
-  __shared__ float mx[64], sm[64];
+  __shared__ float mx[2 * kMaxGammaSample + 1], sm[2 * kMaxGammaSample + 1];
+  __shared__ float pj[kMaxGammaSample], qj[kMaxGammaSample], uj[kMaxGammaSample];
+  __shared__ int okj[kMaxGammaSample];
   pdl_launch_dependents();
   pdl_wait();
   const int b = blockIdx.x, R = gamma + 1, nrow = 2 * gamma + 1;
-  const int r = threadIdx.x;
-  if (r < nrow) {  // combine the row's chunks in ascending order
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = w; r < nrow; r += blockDim.x >> 5) {
     const float2* pp = partials + (static_cast<size_t>(b) * nrow + r) * n_chunks;
-    float m = -INFINITY;
-    for (int c = 0; c < n_chunks; ++c) m = fmaxf(m, pp[c].x);
-    float s = 0.f;
-    for (int c = 0; c < n_chunks; ++c)
-      if (pp[c].y > 0.f) s += pp[c].y * expf(pp[c].x - m);
-    mx[r] = m;
-    sm[r] = s;
+    float m = -INFINITY, s = 0.f;
+    for (int c = lane; c < n_chunks; c += 32) softmax_merge(m, s, pp[c].x, pp[c].y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      // both lanes of a pair merge in the same (lower lane first) order
+      if (lane & o) { float tm = m, ts = s; m = m2; s = s2; softmax_merge(m, s, tm, ts); }
+      else softmax_merge(m, s, m2, s2);
+    }
+    if (lane == 0) { mx[r] = m; sm[r] = s; }
+  }
+  __syncthreads();
+  const int j = threadIdx.x;
+  if (j < gamma) {
+    const int x = draft[static_cast<size_t>(b) * gamma + j];
+    const bool ok = x >= 0 && x < V;  // not a token: rejected
+    okj[j] = ok;
+    pj[j] = ok ? expf(logit_at(target, (static_cast<size_t>(b) * R + j) * V + x) * inv_t - mx[j]) / sm[j] : 0.f;
+    qj[j] = ok ? expf(draft_logits[(static_cast<size_t>(b) * gamma + j) * V + x] * inv_t - mx[R + j]) / sm[R + j]
+               : 1.f;
+    uj[j] = rng_uniform(seed, rng_counter(kStreamAccept, j, b, 0));
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int a = 0;
-    for (; a < gamma; ++a) {
-      const int x = draft[static_cast<size_t>(b) * gamma + a];
-      if (x < 0 || x >= V) break;  // not a token: rejected
-      const float p = expf(logit_at(target, (static_cast<size_t>(b) * R + a) * V + x) / temp - mx[a]) / sm[a];
-      const float q =
-          expf(draft_logits[(static_cast<size_t>(b) * gamma + a) * V + x] / temp - mx[R + a]) / sm[R + a];
-      const float u = rng_uniform(seed, rng_counter(kStreamAccept, a, b, 0));
-      if (!(u * q < p)) break;
-    }
+    while (a < gamma && okj[a] && uj[a] * qj[a] < pj[a]) ++a;
     SampleState st{};
     st.a = a;
     st.mt = mx[a];
@@ -164,7 +188,7 @@ __global__ void __launch_bounds__(64)
 template <typename TT>
 __global__ void __launch_bounds__(kStatThreads)
     sample_resid_kernel(const TT* target, const float* draft_logits, const int32_t* draft, int gamma,
-                        int V, float temp, uint64_t seed, int n_chunks, const SampleState* state,
+                        int V, float inv_t, uint64_t seed, int n_chunks, const SampleState* state,
                         unsigned long long* keys, unsigned int* counters, int32_t* tau,
                         int32_t* committed, int32_t* next_anchor) {
   __shared__ unsigned long long red[8];
@@ -178,13 +202,13 @@ __global__ void __launch_bounds__(kStatThreads)
   const size_t drow = (static_cast<size_t>(b) * gamma + (a < gamma ? a : 0)) * V;
   unsigned long long best_r = 0ull, best_f = 0ull;  // residual draw, plain draw
 #pragma unroll 4
-  for (int i = 0; i < kPerThread; ++i) {
-    const int v = c * kSampChunk + threadIdx.x + i * kStatThreads;
+  for (int i = 0; i < kResidPer; ++i) {
+    const int v = c * kResidChunk + threadIdx.x + i * kStatThreads;
     if (v >= V) break;
-    const float tv = logit_at(target, trow + v) / temp;
+    const float tv = logit_at(target, trow + v) * inv_t;
     if (a < gamma) {
       const float g = rng_gumbel(seed, rng_counter(kStreamResid, a, b, static_cast<uint32_t>(v)));
-      const float w = expf(tv - st.mt) / st.st - expf(draft_logits[drow + v] / temp - st.md) / st.sd;
+      const float w = expf(tv - st.mt) / st.st - expf(draft_logits[drow + v] * inv_t - st.md) / st.sd;
       if (w > 0.f) {
         const unsigned long long k = argmax_key(logf(w) + g, static_cast<uint32_t>(v));
         best_r = k > best_r ? k : best_r;
@@ -259,15 +283,17 @@ cudaError_t launch_all(const TT* target, const float* draft_logits, const int32_
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(base + L.keys);
   unsigned int* counters = reinterpret_cast<unsigned int*>(base + L.counters);
   const int n_chunks = (V + kSampChunk - 1) / kSampChunk;
+  const int n_resid = (V + kResidChunk - 1) / kResidChunk;
+  const float inv_t = 1.0f / temp;  // logits are scaled by 1/T in every kernel alike
   cudaError_t e = launch_ex(sample_stats_kernel<TT>, dim3(n_chunks, B * (2 * gamma + 1)),
-                            dim3(kStatThreads), s, pdl, target, draft_logits, gamma, V, temp, n_chunks,
+                            dim3(kStatThreads), s, pdl, target, draft_logits, gamma, V, inv_t, n_chunks,
                             partials);
   if (e != cudaSuccess) return e;
-  e = launch_ex(sample_decide_kernel<TT>, dim3(B), dim3(64), s, pdl, target, draft_logits, draft, gamma, V,
-                temp, seed, n_chunks, static_cast<const float2*>(partials), state, keys, counters);
+  e = launch_ex(sample_decide_kernel<TT>, dim3(B), dim3(1024), s, pdl, target, draft_logits, draft, gamma, V,
+                inv_t, seed, n_chunks, static_cast<const float2*>(partials), state, keys, counters);
   if (e != cudaSuccess) return e;
-  return launch_ex(sample_resid_kernel<TT>, dim3(n_chunks, B), dim3(kStatThreads), s, pdl, target,
-                   draft_logits, draft, gamma, V, temp, seed, n_chunks,
+  return launch_ex(sample_resid_kernel<TT>, dim3(n_resid, B), dim3(kStatThreads), s, pdl, target,
+                   draft_logits, draft, gamma, V, inv_t, seed, n_resid,
                    static_cast<const SampleState*>(state), keys, counters, tau, committed, next_anchor);
 }
 
