@@ -118,7 +118,8 @@ class DraftCycle:
     def __init__(self, dfl, wl: synth.Workload, device: str):
         self.dfl, self.wl, self.dev = dfl, wl, device
         R, B = wl.rows, wl.batch
-        self.cfg = dfl.config_from_workload(wl)
+        # capacity in whole 128-key pages, so that the paged variant covers the same positions
+        self.cfg = dfl.config_from_workload(wl, ctx_capacity=(wl.capacity() + 127) // 128 * 128)
         self.W = synth.weights(wl, device)
         self.w = dfl.Weights(self.cfg, self.W, device)
         prefix = synth.ctx_lengths(wl) - R          # context before the step's injection
@@ -208,6 +209,45 @@ class DraftCycle:
                                  self.k_cache, self.v_cache, self.draft, self.status, self.ws, trace=trace)
         d.dflash_verify_accept_dyn(self.cfg, self.target, self.draft, self.v_gamma, self.tau, self.committed,
                                    self.next_anchor, self.ws, trace=trace)
+
+    def _paged_state(self):
+        """Page pools holding the same prefix as the contiguous cache, pages
+        placed in a scrambled order (built once, outside any timing)."""
+        if hasattr(self, "pages"):
+            return
+        d, wl, dev = self.dfl, self.wl, self.dev
+        B, page = wl.batch, d.PAGE_KEYS
+        pps = self.cfg.ctx_capacity // page
+        n_pages = B * pps + 3
+        table = np.random.default_rng(5).permutation(n_pages)[: B * pps].reshape(B, pps).astype(np.int32)
+        shape = (wl.n_layers, n_pages, wl.n_kv_heads, page, wl.head_dim)
+        dt = synth.torch_dtype(wl.dtype)
+        self.k_pool = torch.zeros(shape, dtype=dt, device=dev)
+        self.v_pool = torch.zeros(shape, dtype=dt, device=dev)
+        self.pages = d.KvPages(self.k_pool, self.v_pool, torch.as_tensor(table, device=dev))
+        tmax = int(self.prefix.max())
+        taps = synth.taps(wl, B * tmax, "prefill", dev).view(B, tmax, -1)
+        h = torch.empty((B, tmax, wl.d_model), dtype=dt, device=dev)
+        for b in range(B):
+            d.dflash_ctx_fuse(self.cfg, self.w, taps[b, : int(self.prefix[b])], h[b], self.ws)
+        self.ctx_len_p = torch.zeros(B, dtype=torch.int32, device=dev)
+        d.dflash_kv_inject_paged(self.cfg, self.w, h, torch.as_tensor(self.prefix, device=dev), self.ctx_len_p,
+                                 self.pages, self.status, self.ws)
+        self.ctx0_p = self.ctx_len_p.clone()
+        torch.cuda.synchronize()
+
+    def step_paged(self, trace=None):
+        """The greedy cycle over a paged KV cache."""
+        d, wl = self.dfl, self.wl
+        self._paged_state()
+        self.ctx_len_p.copy_(self.ctx0_p)
+        d.dflash_ctx_fuse(self.cfg, self.w, self.step_taps, self.h_new.view(-1, wl.d_model), self.ws,
+                          trace=trace)
+        d.dflash_kv_inject_paged(self.cfg, self.w, self.h_new, self.n_new, self.ctx_len_p, self.pages,
+                                 self.status, self.ws, trace=trace)
+        d.dflash_draft_block_paged(self.cfg, self.w, self.anchor, self.ctx_len_p, self.max_ctx, self.pages,
+                                   self.draft, self.status, self.ws, trace=trace)
+        self.step_verify(trace)
 
     def step_unmask(self, trace=None, n_steps=4):
         """Multi-step confidence unmasking (n_steps passes), greedy verification."""
@@ -504,6 +544,8 @@ def run_gpu(args):
                                             what=f"block size {gam // 2} of {gam} per sequence"),
             "unmask_4_passes": dict(measure_variant(cyc, cyc.step_unmask, min(args.steps, 20), B * gam, hbm),
                                     what="multi-step confidence unmasking, 4 passes"),
+            "paged_kv": dict(measure_variant(cyc, cyc.step_paged, min(args.steps, 50), B * gam, hbm),
+                             what="greedy cycle over a paged KV cache (128-key pages, scrambled)"),
         }
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

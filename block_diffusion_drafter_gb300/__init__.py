@@ -52,6 +52,22 @@ class Trace(ctypes.Structure):
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
+PAGE_KEYS = 128
+
+
+class KvPages(ctypes.Structure):
+    """dflash_kv_pages: page pools [L, n_pages, Hkv, 128, Dh] and a device page
+    table [max_batch, pages_per_seq] (tensors kept alive by the object)."""
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("n_pages", ctypes.c_int),
+                ("pages_per_seq", ctypes.c_int)]
+
+    def __init__(self, k_pool, v_pool, page_table):
+        super().__init__(k_pool.data_ptr(), v_pool.data_ptr(), page_table.data_ptr(), k_pool.shape[1],
+                         page_table.shape[1])
+        self._keep = (k_pool, v_pool, page_table)
+
+
 _SIGS = {
     "dflash_abi_version": (_I, []),
     "dflash_status_string": (ctypes.c_char_p, [_I]),
@@ -82,6 +98,10 @@ _SIGS = {
                                 _P]),
     "dflash_draft_block_iter": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _I, _I,
                                      _P, _P, _I, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
+    "dflash_kv_inject_paged": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _I, _I, _P,
+                                    ctypes.POINTER(KvPages), _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
+    "dflash_draft_block_paged": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _I, _I,
+                                      ctypes.POINTER(KvPages), _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
     "dflash_draft_block_sample": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P,
                                        _I, _I, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P,
                                        _P, _SZ, ctypes.POINTER(Trace), _P]),
@@ -257,6 +277,24 @@ def dflash_verify_accept(cfg, target_logits, draft, tau, committed, next_anchor,
     _check("dflash_verify_accept", load().dflash_verify_accept(
         ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), B, _ptr(tau), _ptr(committed),
         _ptr(next_anchor), ws.ptr, ws.nbytes,
+        ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_kv_inject_paged(cfg, w: Weights, h_ctx, n_new, ctx_len, pages: KvPages, dev_status, ws: Workspace,
+                           trace=None, stream=None):
+    B, Tmax = h_ctx.shape[0], h_ctx.shape[1]
+    _check("dflash_kv_inject_paged", load().dflash_kv_inject_paged(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(h_ctx), _ptr(n_new), B, Tmax, _ptr(ctx_len),
+        ctypes.byref(pages), _ptr(dev_status), ws.ptr, ws.nbytes,
+        ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_draft_block_paged(cfg, w: Weights, anchor, ctx_len, max_ctx_hint, pages: KvPages, draft, dev_status,
+                             ws: Workspace, logits=None, trace=None, stream=None):
+    B = anchor.shape[0]
+    _check("dflash_draft_block_paged", load().dflash_draft_block_paged(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(anchor), _ptr(ctx_len), B, int(max_ctx_hint),
+        ctypes.byref(pages), _ptr(draft), _ptr(logits), _ptr(dev_status), ws.ptr, ws.nbytes,
         ctypes.byref(trace) if trace is not None else None, _stream(stream)))
 
 

@@ -34,9 +34,16 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
   const int n_keys = p.ctx_len[b] + r_b;
   const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
   const float* q = reinterpret_cast<const float*>(p.q) + (static_cast<size_t>(b) * p.R + i) * hq_stride + hq * DH;
-  const size_t kv_base = (static_cast<size_t>(b) * p.n_kv_heads + kvh) * p.ncap * DH;
-  const float* kg = reinterpret_cast<const float*>(p.k_cache) + kv_base;
-  const float* vg = reinterpret_cast<const float*>(p.v_cache) + kv_base;
+  const float* kg = reinterpret_cast<const float*>(p.k_cache);   // this layer's cache or page pool
+  const float* vg = reinterpret_cast<const float*>(p.v_cache);
+  // element offset of key j (paged: through the page table)
+  auto key_off = [&](int j) -> size_t {
+    if (p.page_table == nullptr)
+      return ((static_cast<size_t>(b) * p.n_kv_heads + kvh) * p.ncap + j) * DH;
+    int pg = p.page_table[static_cast<size_t>(b) * p.pages_per_seq + j / kPageKeys];
+    if (pg < 0 || pg >= p.n_pages) pg = 0;  // reported by whoever wrote the row
+    return ((static_cast<size_t>(pg) * p.n_kv_heads + kvh) * kPageKeys + (j % kPageKeys)) * DH;
+  };
   float qv[DH];
 #pragma unroll
   for (int d = 0; d < DH; ++d) qv[d] = q[d];
@@ -45,7 +52,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
 #pragma unroll
   for (int d = 0; d < DH; ++d) o[d] = 0.f;
   for (int j = threadIdx.x; j < n_keys; j += blockDim.x) {
-    const float* kr = kg + static_cast<size_t>(j) * DH;
+    const size_t off = key_off(j);
+    const float* kr = kg + off;
     float sdot = 0.f;
 #pragma unroll
     for (int d = 0; d < DH; ++d) sdot += qv[d] * kr[d];
@@ -54,7 +62,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
     const float al = m == -INFINITY ? 0.f : exp2f(m - mn);
     const float pj = exp2f(sdot - mn);
     l = l * al + pj;
-    const float* vr = vg + static_cast<size_t>(j) * DH;
+    const float* vr = vg + off;
 #pragma unroll
     for (int d = 0; d < DH; ++d) o[d] = o[d] * al + pj * vr[d];
     m = mn;
@@ -115,7 +123,9 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   if (a.bf16) return launch_attention_tc(a, stream, pdl);
   if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
   // fp32: the per-layer slice of the caches
-  const size_t layer_elems = static_cast<size_t>(a.max_batch) * a.n_kv_heads * a.ncap * a.head_dim;
+  const size_t layer_elems = a.page_table != nullptr
+                                 ? static_cast<size_t>(a.n_pages) * a.n_kv_heads * kPageKeys * a.head_dim
+                                 : static_cast<size_t>(a.max_batch) * a.n_kv_heads * a.ncap * a.head_dim;
   AttnArgs al = a;
   al.k_cache = static_cast<const float*>(a.k_cache) + layer_elems * a.layer;
   al.v_cache = static_cast<const float*>(a.v_cache) + layer_elems * a.layer;

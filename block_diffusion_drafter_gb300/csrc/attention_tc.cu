@@ -143,11 +143,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t bar = smem_u32(&hdr->kv_full[st]);
         const uint32_t kd = kv_s + st * kKVBytes, vd = kd + NSUB * kSub;
         const int kb = k_begin + t * kTileKeys;
+        int z = slab, y = kb;
+        if (p.page_table != nullptr) {  // the tile is one page of the pool
+          int pg = p.page_table[static_cast<size_t>(b) * p.pages_per_seq + kb / kPageKeys];
+          if (pg < 0 || pg >= p.n_pages) {
+            report(p.dev_status, DFLASH_ERR_CAPACITY);
+            pg = 0;
+          }
+          z = (p.layer * p.n_pages + pg) * p.n_kv_heads + kvh;
+          y = 0;
+        }
         mbar_expect_tx(bar, kKVBytes);
 #pragma unroll
         for (int j = 0; j < NSUB; ++j) {
-          tma_load_3d(kd + j * kSub, &k_map, bar, 64 * j, kb, slab, pol);
-          tma_load_3d(vd + j * kSub, &v_map, bar, 64 * j, kb, slab, pol);
+          tma_load_3d(kd + j * kSub, &k_map, bar, 64 * j, y, z, pol);
+          tma_load_3d(vd + j * kSub, &v_map, bar, 64 * j, y, z, pol);
         }
       }
     }
@@ -444,11 +454,14 @@ namespace dfl {
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
   if ((a.n_q_heads / a.n_kv_heads) * a.R > 128 || a.splits > kMaxCluster) return cudaErrorInvalidValue;
-  // one tensor map per cache over all layers: [L * max_batch * Hkv][Ncap][Dh]
+  // one tensor map per cache over all layers: [L * max_batch * Hkv][Ncap][Dh],
+  // or for page pools [L * n_pages * Hkv][kPageKeys][Dh] (a tile is a page)
   CUtensorMap km, vm;
-  const uint64_t slabs = static_cast<uint64_t>(a.n_layers) * a.max_batch * a.n_kv_heads;
-  if (!make_operand_map(&km, a.k_cache, 2, a.head_dim, a.ncap, slabs, kTileKeys) ||
-      !make_operand_map(&vm, a.v_cache, 2, a.head_dim, a.ncap, slabs, kTileKeys))
+  const bool paged = a.page_table != nullptr;
+  const uint64_t slabs = static_cast<uint64_t>(a.n_layers) * (paged ? a.n_pages : a.max_batch) * a.n_kv_heads;
+  const uint64_t rows = paged ? kPageKeys : a.ncap;
+  if (!make_operand_map(&km, a.k_cache, 2, a.head_dim, rows, slabs, kTileKeys) ||
+      !make_operand_map(&vm, a.v_cache, 2, a.head_dim, rows, slabs, kTileKeys))
     return cudaErrorInvalidValue;
   const int nsub = a.head_dim / 64;
   const size_t smem = sizeof(AttnSmem) + 1024 + static_cast<size_t>(nsub) * kSub + 2 * kSub +

@@ -271,14 +271,23 @@ Epi base_epi(const dflash_config* c) {
   return e;
 }
 
+// A page view: both pools, a table, at least one page and the block's
+// reserve within one sequence's pages.
+bool pages_ok(const dflash_config* c, const dflash_kv_pages* p) {
+  return p != nullptr && p->k_pool != nullptr && p->v_pool != nullptr && p->page_table != nullptr &&
+         p->n_pages >= 1 && p->pages_per_seq >= 1 &&
+         static_cast<long long>(p->pages_per_seq) * DFLASH_PAGE_KEYS >= c->gamma + 2;
+}
+
 bool trace_ok(const dflash_trace* t) {
   return t == nullptr || (t->events != nullptr && t->kinds != nullptr && t->bytes != nullptr &&
                           t->flops != nullptr && t->capacity >= 0);
 }
 
-bool rope_ok(const dflash_config* c, const dflash_weights* w) {
+// RoPE tables cover every position a sequence of capacity ncap can reach.
+bool rope_ok(const dflash_config* c, const dflash_weights* w, int ncap) {
   if (c->rope_theta == 0.f) return true;
-  return w->rope_cos != nullptr && w->rope_sin != nullptr && w->rope_positions >= c->ctx_capacity;
+  return w->rope_cos != nullptr && w->rope_sin != nullptr && w->rope_positions >= ncap;
 }
 
 }  // namespace
@@ -390,16 +399,18 @@ dflash_status dflash_ctx_fuse(const dflash_config* c, const dflash_weights* w, c
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
-dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, const void* h_ctx,
-                               const int32_t* n_new, int B, int Tmax, int32_t* ctx_len, void* k_cache,
-                               void* v_cache, int32_t* dev_status, void* ws, size_t ws_bytes,
-                               dflash_trace* trace, dflash_stream_t stream) {
+static dflash_status kv_inject_impl(const dflash_config* c, const dflash_weights* w, const void* h_ctx,
+                                    const int32_t* n_new, int B, int Tmax, int32_t* ctx_len, void* k_cache,
+                                    void* v_cache, const dflash_kv_pages* pages, int32_t* dev_status, void* ws,
+                                    size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
+  // capacity per sequence: the contiguous cache's, or the pages of its table
+  const int ncap = pages != nullptr ? pages->pages_per_seq * DFLASH_PAGE_KEYS : c->ctx_capacity;
   if (w == nullptr || B < 0 || B > c->max_batch || Tmax < 0) return DFLASH_ERR_INVALID_ARG;
   if (B == 0 || Tmax == 0) return DFLASH_OK;
   if (h_ctx == nullptr || n_new == nullptr || ctx_len == nullptr || k_cache == nullptr ||
-      v_cache == nullptr || dev_status == nullptr || w->w_qkv == nullptr || !rope_ok(c, w) ||
+      v_cache == nullptr || dev_status == nullptr || w->w_qkv == nullptr || !rope_ok(c, w, ncap) ||
       !trace_ok(trace))
     return DFLASH_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c);
@@ -442,6 +453,12 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
   g.epi.op = EPI_KV;
   g.epi.k_cache = k_cache;
   g.epi.v_cache = v_cache;
+  g.epi.ncap = ncap;
+  if (pages != nullptr) {
+    g.epi.page_table = pages->page_table;
+    g.epi.n_pages = pages->n_pages;
+    g.epi.pages_per_seq = pages->pages_per_seq;
+  }
   g.epi.ctx_len = ctx_len;
   g.epi.n_new = n_new;
   g.epi.rows_per_seq = Tmax;
@@ -456,10 +473,27 @@ dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, 
   if ((st = run_gemm(cx, g, amap, bmap, plan, bytes, 2.0 * rows * c->n_layers * static_cast<double>(fpl) * D)) != DFLASH_OK)
     return st;
   cx.tr.before(DFLASH_K_NORM, 12.0 * B, 0);
-  const cudaError_t e = launch_kv_advance(ctx_len, n_new, B, Tmax, c->ctx_capacity, c->gamma + 1,
-                                          dev_status, cx.s, cx.pdl);
+  const cudaError_t e = launch_kv_advance(ctx_len, n_new, B, Tmax, ncap, c->gamma + 1, dev_status, cx.s,
+                                          cx.pdl);
   cx.tr.after();
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+dflash_status dflash_kv_inject(const dflash_config* c, const dflash_weights* w, const void* h_ctx,
+                               const int32_t* n_new, int B, int Tmax, int32_t* ctx_len, void* k_cache,
+                               void* v_cache, int32_t* dev_status, void* ws, size_t ws_bytes,
+                               dflash_trace* trace, dflash_stream_t stream) {
+  return kv_inject_impl(c, w, h_ctx, n_new, B, Tmax, ctx_len, k_cache, v_cache, nullptr, dev_status, ws,
+                        ws_bytes, trace, stream);
+}
+
+dflash_status dflash_kv_inject_paged(const dflash_config* c, const dflash_weights* w, const void* h_ctx,
+                                     const int32_t* n_new, int B, int Tmax, int32_t* ctx_len,
+                                     const dflash_kv_pages* pages, int32_t* dev_status, void* ws, size_t ws_bytes,
+                                     dflash_trace* trace, dflash_stream_t stream) {
+  if (!pages_ok(c, pages)) return DFLASH_ERR_INVALID_ARG;
+  return kv_inject_impl(c, w, h_ctx, n_new, B, Tmax, ctx_len, pages->k_pool, pages->v_pool, pages, dev_status,
+                        ws, ws_bytes, trace, stream);
 }
 
 }  // extern "C"
@@ -471,14 +505,16 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
                                       int max_ctx_hint, void* k_cache,
                                       void* v_cache, float temperature, uint64_t seed, int32_t* draft,
                                       float* logits_opt, float* layer_dump_opt, int32_t* dev_status, void* ws,
-                                      size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
+                                      size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream,
+                                      const dflash_kv_pages* pages = nullptr) {
+  const int ncap = pages != nullptr ? pages->pages_per_seq * DFLASH_PAGE_KEYS : c->ctx_capacity;
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
   if (w == nullptr || B < 1 || B > c->max_batch || max_ctx_hint < 0) return DFLASH_ERR_INVALID_ARG;
   if ((anchor == nullptr && ids == nullptr) || ctx_len == nullptr || k_cache == nullptr || v_cache == nullptr ||
       draft == nullptr || dev_status == nullptr || w->embed == nullptr || w->g_final == nullptr ||
       w->lm_head == nullptr || w->g_attn == nullptr || w->w_qkv == nullptr || w->w_o == nullptr ||
-      w->g_ffn == nullptr || w->w_gateup == nullptr || w->w_down == nullptr || !rope_ok(c, w))
+      w->g_ffn == nullptr || w->w_gateup == nullptr || w->w_down == nullptr || !rope_ok(c, w, ncap))
     return DFLASH_ERR_INVALID_ARG;
   if (!trace_ok(trace)) return DFLASH_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(c);
@@ -585,7 +621,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
     return DFLASH_ERR_CUDA;
 
   int a_splits = 1, a_chunk = 0;
-  plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, c->ctx_capacity,
+  plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, ncap,
                  &a_splits, &a_chunk);
 
   for (int l = 0; l < Lyr; ++l) {
@@ -598,6 +634,12 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
       g.epi = base_epi(c);
       g.epi.op = EPI_QKV; g.epi.out = q; g.epi.ld = HD; g.epi.n_tok = rows; g.epi.n_feat = nqkv;
       g.epi.k_cache = k_cache; g.epi.v_cache = v_cache; g.epi.ctx_len = ctx_len;
+      g.epi.ncap = ncap;
+      if (pages != nullptr) {
+        g.epi.page_table = pages->page_table;
+        g.epi.n_pages = pages->n_pages;
+        g.epi.pages_per_seq = pages->pages_per_seq;
+      }
       g.epi.rows_per_seq = R; g.epi.layer = l;
       g.epi.rope_cos = c->rope_theta > 0.f ? w->rope_cos : nullptr;
       g.epi.rope_sin = c->rope_theta > 0.f ? w->rope_sin : nullptr;
@@ -619,7 +661,12 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
       a.out_lo_off = ao_lo;
       a.dev_status = dev_status;
       a.B = B; a.R = R; a.n_q_heads = c->n_q_heads; a.n_kv_heads = c->n_kv_heads;
-      a.head_dim = c->head_dim; a.ncap = c->ctx_capacity; a.max_batch = c->max_batch;
+      a.head_dim = c->head_dim; a.ncap = ncap; a.max_batch = c->max_batch;
+      if (pages != nullptr) {
+        a.page_table = pages->page_table;
+        a.n_pages = pages->n_pages;
+        a.pages_per_seq = pages->pages_per_seq;
+      }
       a.splits = a_splits; a.chunk = a_chunk; a.bf16 = bf16;
       const double kvb = 2.0 * B * c->n_kv_heads * static_cast<double>(max_ctx_hint + R) * c->head_dim * es;
       const double fl = 4.0 * B * c->n_q_heads * R * static_cast<double>(max_ctx_hint + R) * c->head_dim;
@@ -708,6 +755,15 @@ dflash_status dflash_draft_block(const dflash_config* c, const dflash_weights* w
                                  dflash_trace* trace, dflash_stream_t stream) {
   return draft_block_impl(c, w, anchor, nullptr, ctx_len, nullptr, B, max_ctx_hint, k_cache, v_cache, 0.f, 0, draft,
                           logits_opt, layer_dump_opt, dev_status, ws, ws_bytes, trace, stream);
+}
+
+dflash_status dflash_draft_block_paged(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,
+                                       const int32_t* ctx_len, int B, int max_ctx_hint, const dflash_kv_pages* pages,
+                                       int32_t* draft, float* logits_opt, int32_t* dev_status, void* ws,
+                                       size_t ws_bytes, dflash_trace* trace, dflash_stream_t stream) {
+  if (!pages_ok(c, pages)) return DFLASH_ERR_INVALID_ARG;
+  return draft_block_impl(c, w, anchor, nullptr, ctx_len, nullptr, B, max_ctx_hint, pages->k_pool, pages->v_pool,
+                          0.f, 0, draft, logits_opt, nullptr, dev_status, ws, ws_bytes, trace, stream, pages);
 }
 
 dflash_status dflash_draft_block_dyn(const dflash_config* c, const dflash_weights* w, const int32_t* anchor,

@@ -111,6 +111,16 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           const int nn = e.n_new[seq];
           if (t < nn && base + nn <= e.ncap - e.reserve) pos = base + t;
         }
+        // paged caches: the slot of the token table holds the row's page
+        if (pos >= 0 && e.page_table != nullptr) {
+          const int pg = e.page_table[static_cast<size_t>(seq) * e.pages_per_seq + pos / kPageKeys];
+          if (pg < 0 || pg >= e.n_pages) {
+            report(g.dev_status, DFLASH_ERR_CAPACITY);
+            pos = -1;
+          } else {
+            seq = pg;
+          }
+        }
       }
       ti->pos[x] = pos;
       ti->seq[x] = seq;
@@ -280,7 +290,12 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
               const bool is_k = f < nq + nk;
               const int head = (is_k ? f - nq : f - nq - nk) / Dh;
               kind[u] = is_k ? 2 : 3;
-              o[u] = (((static_cast<size_t>(layer) * e.max_batch + seq) * e.n_kv_heads + head) * e.ncap + pos) * Dh + d;
+              // seq: the sequence, or for paged caches the row's page
+              o[u] = e.page_table != nullptr
+                         ? (((static_cast<size_t>(layer) * e.n_pages + seq) * e.n_kv_heads + head) * kPageKeys +
+                            pos % kPageKeys) * Dh + d
+                         : (((static_cast<size_t>(layer) * e.max_batch + seq) * e.n_kv_heads + head) * e.ncap + pos) *
+                                   Dh + d;
             }
             if (kind[u] == 1 && tok >= e.n_tok) kind[u] = 0;
             if (kind[u] != 0) {

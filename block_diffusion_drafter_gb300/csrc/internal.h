@@ -12,6 +12,7 @@ namespace dfl {
 
 constexpr int kBM = 128;        // MMA M: rows of the A operand per tile
 constexpr int kMaxBN = 512;     // B-operand rows per tile (two MMAs of <= 256)
+constexpr int kPageKeys = 128;  // keys per KV-cache page (one attention tile)
 constexpr int kGemmThreads = 192;
 
 // Epilogue operations of the projection GEMM.
@@ -41,6 +42,12 @@ struct Epi {
   int layer;          // EPI_QKV: layer; EPI_KV: layer of feature tile 0 (see feat_per_layer)
   int feat_per_layer; // EPI_KV: 2*Hkv*Dh features per layer (layer = feat / feat_per_layer)
   int max_batch, n_q_heads, n_kv_heads, head_dim, ncap, reserve;
+  // paged caches (page_table != NULL): k_cache / v_cache are page pools
+  // [L][n_pages][Hkv][kPageKeys][Dh]; key p of sequence s lives in page
+  // page_table[s * pages_per_seq + p / kPageKeys], row p % kPageKeys; ncap is
+  // then pages_per_seq * kPageKeys
+  const int32_t* page_table;
+  int n_pages, pages_per_seq;
   const float* rope_cos;
   const float* rope_sin;
   int rope_positions;
@@ -134,6 +141,8 @@ struct AttnArgs {
   int splits, chunk;      // keys per split (multiple of 64); last split takes the rest;
                           // the splits of one (sequence, KV head) form one cluster
   int bf16;
+  const int32_t* page_table;   // NULL, or paged caches as in Epi
+  int n_pages, pages_per_seq;
 };
 void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
                     int* chunk);

@@ -130,6 +130,29 @@ typedef struct {
   double* flops;   /* host [capacity] algorithmic flops per launch     */
 } dflash_trace;
 
+/* Paged KV cache (SURVEY's NEXT row "paged / ragged KV-cache layout" for
+ * serving-style continuous batching; the pages describe the cache only as
+ * computed once per position and reused, [P1] "추론 구조"). Each layer's K
+ * and V live in a pool of pages of DFLASH_PAGE_KEYS positions:
+ *   pool[L][n_pages][Hkv][DFLASH_PAGE_KEYS][Dh]  (cfg.dtype)
+ * and position p of sequence b in page page_table[b * pages_per_seq + p /
+ * DFLASH_PAGE_KEYS], row p % DFLASH_PAGE_KEYS. A sequence's capacity is
+ * pages_per_seq * DFLASH_PAGE_KEYS positions (replacing cfg.ctx_capacity for
+ * the *_paged calls; the last gamma + 1 of them are the draft block's
+ * scratch rows, as in the contiguous cache). The caller owns the pools and
+ * the table and allocates pages before positions reach them; a write or
+ * read through an entry outside [0, n_pages) sets DFLASH_ERR_CAPACITY in
+ * dev_status (writes are skipped). Every page covers one 128-key attention
+ * tile, so a tile is a single TMA box wherever the page sits in the pool. */
+#define DFLASH_PAGE_KEYS 128
+typedef struct {
+  void* k_pool;               /* device [L, n_pages, Hkv, DFLASH_PAGE_KEYS, Dh] */
+  void* v_pool;               /* device, same shape                              */
+  const int32_t* page_table;  /* device [max_batch, pages_per_seq] page ids      */
+  int n_pages;                /* pages in each pool                              */
+  int pages_per_seq;          /* table entries per sequence                      */
+} dflash_kv_pages;
+
 /* ABI version compiled into the library (DFLASH_ABI_VERSION). */
 int dflash_abi_version(void);
 
@@ -219,6 +242,22 @@ dflash_status dflash_draft_block(const dflash_config* cfg, const dflash_weights*
                                  float* layer_dump_opt, int32_t* dev_status,
                                  void* ws, size_t ws_bytes, dflash_trace* trace,
                                  dflash_stream_t stream);
+
+/* dflash_kv_inject and dflash_draft_block over a paged KV cache
+ * (dflash_kv_pages): the same computation, with every cache row addressed
+ * through the page table. The RoPE tables must cover the paged capacity.
+ * Results equal the contiguous calls' bit for bit. */
+dflash_status dflash_kv_inject_paged(const dflash_config* cfg, const dflash_weights* w,
+                                     const void* h_ctx, const int32_t* n_new, int B, int Tmax,
+                                     int32_t* ctx_len, const dflash_kv_pages* pages,
+                                     int32_t* dev_status, void* ws, size_t ws_bytes,
+                                     dflash_trace* trace, dflash_stream_t stream);
+dflash_status dflash_draft_block_paged(const dflash_config* cfg, const dflash_weights* w,
+                                       const int32_t* anchor, const int32_t* ctx_len, int B,
+                                       int max_ctx_hint, const dflash_kv_pages* pages,
+                                       int32_t* draft, float* logits_opt, int32_t* dev_status,
+                                       void* ws, size_t ws_bytes, dflash_trace* trace,
+                                       dflash_stream_t stream);
 
 /* Drafting pass with a block size per sequence (SURVEY's NEXT row "dynamic
  * gamma"; [P1] block-size ablation: a drafter trained with block 16 serves

@@ -171,3 +171,18 @@ def test_unmasking_calls_reject_bad_arguments(lib):
                                          fake, fake, fake, fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
     assert L.dflash_draft_block_ids(ctypes.byref(cfg), ctypes.byref(w), None, fake, 1, 0, fake, fake, fake, None,
                                     fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+
+
+def test_paged_calls_reject_missing_or_short_page_views(lib):
+    L = lib.load()
+    cfg = lib.config_from_workload(synth.WORKLOADS["tiny_f32_L1_N128"])
+    w = lib.WeightsStruct()
+    fake = 256
+    for pages in (None, lib.KvPages.__new__(lib.KvPages)):
+        if pages is not None:   # pools and table set, but no pages
+            ctypes.Structure.__init__(pages, fake, fake, fake, 0, 1)
+        arg = ctypes.byref(pages) if pages is not None else None
+        assert L.dflash_draft_block_paged(ctypes.byref(cfg), ctypes.byref(w), fake, fake, 1, 0, arg, fake, None,
+                                          fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
+        assert L.dflash_kv_inject_paged(ctypes.byref(cfg), ctypes.byref(w), fake, fake, 1, 4, fake, arg, fake, fake,
+                                        1 << 30, None, None) == lib.ERR_INVALID_ARG
