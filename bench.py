@@ -53,6 +53,20 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time, on every rank (replicas finish when the last does)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job drafted tokens/s: every rank drafts its own replica's batch."""
+    return world * tokens_per_step * steps / (ms * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -472,11 +486,8 @@ def run_gpu(args):
     st = int(cyc.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}: {dfl.status_string(st)}")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * tokens * args.steps / (ms * 1e-3)
+    ms = max_over_ranks(ms, world, dev)
+    value = job_throughput(world, tokens, args.steps, ms)
 
     # end to end through host buffers: inputs H2D from pinned memory, results D2H
     h_taps = cyc.step_taps.cpu().pin_memory()
@@ -519,7 +530,7 @@ def run_gpu(args):
         e2e_step()
     if world > 1:
         torch.distributed.barrier()
-    ms_e2e = time_steps(e2e_step, args.steps, stream)
+    ms_e2e = max_over_ranks(time_steps(e2e_step, args.steps, stream), world, dev)
     h2d = h_taps.numel() * h_taps.element_size() + h_target.numel() * 4 + h_anchor.numel() * 4
     d2h = (o_draft.numel() + o_tau.numel() + o_comm.numel()) * 4
 
@@ -566,7 +577,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (weights streamed per step: "
                              f"{step_bytes / 1e9:.2f} GB)", "parallelism": f"replicas x{world}"},
             "clocks": clocks,
-            "e2e": {"value": round(world * tokens * args.steps / (ms_e2e * 1e-3), 1),
+            "e2e": {"value": round(job_throughput(world, tokens, args.steps, ms_e2e), 1),
                     "unit": "drafted tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches * args.steps,
             "roofline": roof,
