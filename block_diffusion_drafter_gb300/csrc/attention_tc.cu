@@ -6,17 +6,21 @@
 // Speculative Decoding 논문 정리", and §3.2 of the marsggbo DFlash page.
 //
 // One CTA owns the G*R query rows of one (sequence, KV head) and a contiguous
-// slice of its keys. Per 128-key tile:
-//   S = Q K^T      tcgen05.mma, Q and K K-major in shared memory, S in TMEM
-//                  with one query row per TMEM lane (= per epilogue thread);
+// slice of its keys. Per 128-key tile t:
+//   S_t = Q K_t^T  tcgen05.mma, Q and K K-major in shared memory, into one of
+//                  two S buffers in TMEM (one query row per TMEM lane = per
+//                  softmax thread), so S_{t+1} is computed while the softmax
+//                  of tile t runs;
 //   softmax        row max / exp2 / row sum are thread-local; the running max
 //                  is raised lazily (O in TMEM is rescaled only when the max
 //                  grows by more than 2^8), P goes to shared memory as bf16;
-//   O += P V       tcgen05.mma with V as an MN-major operand, O in TMEM.
-// K and V tiles stream in by TMA through a 2-stage ring; warp 0 issues TMA,
-// warp 1 the MMAs, warps 2-9 run the softmax (two per TMEM lane quarter). The key slices of one
-// (sequence, KV head) form a thread-block cluster whose partial results are
-// merged through distributed shared memory.
+//   O += P V_t     tcgen05.mma with V as an MN-major operand, O in TMEM.
+// K and V tiles stream in by TMA through two 2-stage rings of their own, so a
+// K stage is refilled as soon as its S product is done. Warp 0 issues TMA
+// (lane 0 K, lane 1 V), warp 1 the MMAs, warps 2-9 run the softmax (two per
+// TMEM lane quarter); a quarter holding no query row only keeps the barrier
+// counts. The key slices of one (sequence, KV head) form a thread-block
+// cluster whose partial results are merged through distributed shared memory.
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -32,8 +36,8 @@ constexpr float kLog2eTc = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.0f;     // log2 units the running max may lag behind
 
 struct AttnSmem {
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t q_full, s_full, s_free, p_full, o_done;
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t q_full, s_full[2], s_free[2], p_full, o_done;
   uint32_t tmem_base;
   int abort_flag;
   float pmax[2][128];  // per-half row max of the current tile
@@ -76,14 +80,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   constexpr int NSUB = DH / 64;                      // 64-dim sub-tiles per head
   constexpr uint32_t kQBytes = NSUB * kSub;
   constexpr uint32_t kPBytes = 2 * kSub;             // 128 keys = two 64-key sub-tiles
-  constexpr uint32_t kKVBytes = 2 * NSUB * kSub;     // K then V of one tile
-  constexpr uint32_t kSCol = 0, kOCol = 128;         // TMEM columns of S and O
+  constexpr uint32_t kTileBytes = NSUB * kSub;       // K or V of one tile
+  constexpr uint32_t kOCol = 256;                    // TMEM columns: S buffers 0 / 128, O 256
+  constexpr uint32_t kTmemCols = 512;
   extern __shared__ uint8_t smem_raw[];
   AttnSmem* hdr = reinterpret_cast<AttnSmem*>(smem_raw);
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + sizeof(AttnSmem) + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_s - raw_s);
-  const uint32_t q_s = base_s, p_s = q_s + kQBytes, kv_s = p_s + kPBytes;
+  const uint32_t q_s = base_s, p_s = q_s + kQBytes, k_s = p_s + kPBytes, v_s = k_s + 2 * kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -92,12 +97,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&hdr->kv_full[i]), 1);
-      mbar_init(smem_u32(&hdr->kv_empty[i]), 1);
+      mbar_init(smem_u32(&hdr->k_full[i]), 1);
+      mbar_init(smem_u32(&hdr->k_empty[i]), 1);
+      mbar_init(smem_u32(&hdr->v_full[i]), 1);
+      mbar_init(smem_u32(&hdr->v_empty[i]), 1);
+      mbar_init(smem_u32(&hdr->s_full[i]), 1);
+      mbar_init(smem_u32(&hdr->s_free[i]), kAttnThreads - 64);
     }
     mbar_init(smem_u32(&hdr->q_full), kAttnThreads - 64);
-    mbar_init(smem_u32(&hdr->s_full), 1);
-    mbar_init(smem_u32(&hdr->s_free), kAttnThreads - 64);
     mbar_init(smem_u32(&hdr->p_full), kAttnThreads - 64);
     mbar_init(smem_u32(&hdr->o_done), 1);
     hdr->abort_flag = 0;
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     fence_proxy_async();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&hdr->tmem_base), 256);
+    tmem_alloc(smem_u32(&hdr->tmem_base), kTmemCols);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -129,19 +136,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* abort_flag = &hdr->abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA producers
+    // lane 0 streams K tiles, lane 1 V tiles, each through its own ring
+    if (lane < 2) {
+      const bool is_v = lane == 1;
+      const CUtensorMap* map = is_v ? &v_map : &k_map;
+      const uint32_t ring = is_v ? v_s : k_s;
       const uint64_t pol = l2_evict_first();
       for (int t = 0; t < nt; ++t) {
         const int st = t & 1, u = t >> 1;
-        if (u > 0 && !mbar_wait(smem_u32(&hdr->kv_empty[st]), (u - 1) & 1)) {
+        const uint32_t empty = smem_u32(is_v ? &hdr->v_empty[st] : &hdr->k_empty[st]);
+        if (u > 0 && !mbar_wait(empty, (u - 1) & 1)) {
           report(p.dev_status, DFLASH_ERR_TIMEOUT);
           atomicExch(&hdr->abort_flag, 1);
           break;
         }
         if (*abort_flag) break;
-        const uint32_t bar = smem_u32(&hdr->kv_full[st]);
-        const uint32_t kd = kv_s + st * kKVBytes, vd = kd + NSUB * kSub;
+        const uint32_t bar = smem_u32(is_v ? &hdr->v_full[st] : &hdr->k_full[st]);
+        const uint32_t dst = ring + st * kTileBytes;
         const int kb = k_begin + t * kTileKeys;
         int z = slab, y = kb;
         if (p.page_table != nullptr) {  // the tile is one page of the pool
@@ -153,37 +165,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           z = (p.layer * p.n_pages + pg) * p.n_kv_heads + kvh;
           y = 0;
         }
-        mbar_expect_tx(bar, kKVBytes);
+        mbar_expect_tx(bar, kTileBytes);
 #pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-          tma_load_3d(kd + j * kSub, &k_map, bar, 64 * j, y, z, pol);
-          tma_load_3d(vd + j * kSub, &v_map, bar, 64 * j, y, z, pol);
-        }
+        for (int j = 0; j < NSUB; ++j) tma_load_3d(dst + j * kSub, map, bar, 64 * j, y, z, pol);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // order: S_0, then per tile t: S_{t+1} (as soon as K_{t+1} is in and its
+    // S buffer was read), P_t V_t (once the softmax wrote P_t)
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc(128, kTileKeys, kFmtBF16);
       const uint32_t idesc_o = make_idesc(128, DH, kFmtBF16, 1);
-      bool ok = nt == 0 || mbar_wait(smem_u32(&hdr->q_full), 0);
-      for (int t = 0; ok && t < nt; ++t) {
+      auto issue_s = [&](int t) -> bool {
         const int st = t & 1, u = t >> 1;
-        ok = mbar_wait(smem_u32(&hdr->kv_full[st]), u & 1) &&
-             (t == 0 || mbar_wait(smem_u32(&hdr->s_free), (t - 1) & 1));
-        if (!ok) break;
+        if (!mbar_wait(smem_u32(&hdr->k_full[st]), u & 1)) return false;
+        if (t >= 2 && !mbar_wait(smem_u32(&hdr->s_free[st]), (u - 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t kt = kv_s + st * kKVBytes, vt = kt + NSUB * kSub;
+        const uint32_t kt = k_s + st * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < DH / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
-          tc_mma_f16(tmem + kSCol, sw128_desc(q_s + off), sw128_desc(kt + off), idesc_s, ks > 0 ? 1u : 0u);
+          tc_mma_f16(tmem + st * kTileKeys, sw128_desc(q_s + off), sw128_desc(kt + off), idesc_s,
+                     ks > 0 ? 1u : 0u);
         }
-        tc_commit(smem_u32(&hdr->s_full));
-        ok = mbar_wait(smem_u32(&hdr->p_full), t & 1);
+        tc_commit(smem_u32(&hdr->s_full[st]));
+        tc_commit(smem_u32(&hdr->k_empty[st]));
+        return true;
+      };
+      bool ok = nt == 0 || (mbar_wait(smem_u32(&hdr->q_full), 0) && issue_s(0));
+      for (int t = 0; ok && t < nt; ++t) {
+        if (t + 1 < nt && !issue_s(t + 1)) { ok = false; break; }
+        const int st = t & 1, u = t >> 1;
+        ok = mbar_wait(smem_u32(&hdr->p_full), t & 1) && mbar_wait(smem_u32(&hdr->v_full[st]), u & 1);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t vt = v_s + st * kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < kTileKeys / 16; ++ks) {
           const uint64_t a = sw128_desc(p_s + (ks >> 2) * kSub + (ks & 3) * 32);
@@ -191,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_mma_f16(tmem + kOCol, a, bd, idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&hdr->o_done));
-        tc_commit(smem_u32(&hdr->kv_empty[st]));
+        tc_commit(smem_u32(&hdr->v_empty[st]));
       }
       if (!ok) {
         report(p.dev_status, DFLASH_ERR_TIMEOUT);
@@ -202,9 +220,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax warps
     // Warps 2..9: TMEM lane quarter (warp % 4) gives the query row; `half`
-    // picks keys 64*half..+63 of each S tile and columns of O.
+    // picks keys 64*half..+63 of each S tile and columns of O. A quarter
+    // without query rows (all q >= n_q) computes nothing.
     const int q = (warp & 3) * 32 + lane;
     const int half = (warp - 2) >> 2;
+    const bool live = (warp & 3) * 32 < n_q;   // warp-uniform
     const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
     const int gq = q / p.R, iq = q % p.R;
@@ -227,39 +247,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
+      const int j = t & 1;
       const int kb = k_begin + t * kTileKeys;
       const int nvalid = min(kTileKeys, k_end - kb);
       const int nv_half = min(HK, max(0, nvalid - half * HK));
-      if (!warp_wait(smem_u32(&hdr->s_full), t & 1)) { ok = false; break; }
-      tc_fence_after();
+      if (!warp_wait(smem_u32(&hdr->s_full[j]), (t >> 1) & 1)) { ok = false; break; }
       float sv[HK];
+      if (live) {
+        tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < HK; c0 += 16) tmem_ld16(t_row + kSCol + half * HK + c0, sv + c0);
-      tmem_ld_wait();
-      if (nv_half < HK) {
-#pragma unroll
-        for (int i = 0; i < HK; ++i)
-          if (i >= nv_half) sv[i] = -INFINITY;
+        for (int c0 = 0; c0 < HK; c0 += 16) tmem_ld16(t_row + j * kTileKeys + half * HK + c0, sv + c0);
+        tmem_ld_wait();
       }
-      float m8[8];
+      // S_t is in registers: its buffer may take S_{t+2}
+      tc_fence_before();
+      mbar_arrive(smem_u32(&hdr->s_free[j]));
+      float m_use = m_run;
+      bool rescale = false;
+      float m_new = m_run;
+      if (live) {
+        if (nv_half < HK) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+          for (int i = 0; i < HK; ++i)
+            if (i >= nv_half) sv[i] = -INFINITY;
+        }
+        float m8[8];
 #pragma unroll
-      for (int i = 8; i < HK; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      // both halves of the row agree on its max
-      hdr->pmax[half][q] = mx;
-      named_bar(2 + (warp & 3), 64);
-      mx = fmaxf(hdr->pmax[0][q], hdr->pmax[1][q]) * scale;
-      const float m_new = fmaxf(m_run, mx);
-      const bool rescale = (m_run == -INFINITY) || (m_new > m_run + kLazyRescale);
-      const float m_use = rescale ? m_new : m_run;
-      // the previous P . V must be done before P is rewritten or O rescaled
+        for (int i = 0; i < 8; ++i) m8[i] = sv[i];
+#pragma unroll
+        for (int i = 8; i < HK; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // both halves of the row agree on its max
+        hdr->pmax[half][q] = mx;
+        named_bar(2 + (warp & 3), 64);
+        mx = fmaxf(hdr->pmax[0][q], hdr->pmax[1][q]) * scale;
+        m_new = fmaxf(m_run, mx);
+        rescale = (m_run == -INFINITY) || (m_new > m_run + kLazyRescale);
+        m_use = rescale ? m_new : m_run;
+      }
+      // the previous P . V must be done before P is rewritten or O rescaled;
+      // every softmax warp waits for it, so that no warp runs ahead and
+      // arrives on p_full for a later tile while this one is still open
       if (t > 0) {
         if (!warp_wait(smem_u32(&hdr->o_done), (t - 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        if (live && __any_sync(0xffffffffu, rescale)) {
           const float alpha = rescale ? exp2_approx(m_run - m_new) : 1.f;
           if (rescale) l_run *= alpha;
           float ov[HO];
@@ -277,37 +310,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (nvalid < kTileKeys) {
         // keys past the end of the slice: zero their V rows (cache rows beyond
         // the context may hold anything, and 0 * NaN would poison O)
-        if (!warp_wait(smem_u32(&hdr->kv_full[t & 1]), (t >> 1) & 1)) { ok = false; break; }
+        if (!warp_wait(smem_u32(&hdr->v_full[j]), (t >> 1) & 1)) { ok = false; break; }
         if (q >= nvalid) {
-          const uint32_t vt = kv_s + (t & 1) * kKVBytes + NSUB * kSub;
+          const uint32_t vt = v_s + j * kTileBytes;
 #pragma unroll
-          for (int j = 0; j < NSUB; ++j)
+          for (int jj = 0; jj < NSUB; ++jj)
 #pragma unroll
             for (int c = half * 4; c < half * 4 + 4; ++c)
-              st_shared_v4(vt + j * kSub + q * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
+              st_shared_v4(vt + jj * kSub + q * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
         }
       }
-      // P = 2^(s * scale - m) as bf16 into sub-tile `half` of the K-major P tile
-      float ls[8];
+      if (live) {
+        // P = 2^(s * scale - m) as bf16 into sub-tile `half` of the K-major P tile
+        float ls[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+        for (int i = 0; i < 8; ++i) ls[i] = 0.f;
 #pragma unroll
-      for (int c = 0; c < HK / 8; ++c) {
-        uint32_t w[4];
+        for (int c = 0; c < HK / 8; ++c) {
+          uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float p0 = exp2_approx(fmaf(sv[c * 8 + i], scale, -m_use));
-          const float p1 = exp2_approx(fmaf(sv[c * 8 + i + 1], scale, -m_use));
-          ls[i] += p0;
-          ls[i + 1] += p1;
-          w[i >> 1] = pack2_bf16(p0, p1);
+          for (int i = 0; i < 8; i += 2) {
+            const float p0 = exp2_approx(fmaf(sv[c * 8 + i], scale, -m_use));
+            const float p1 = exp2_approx(fmaf(sv[c * 8 + i + 1], scale, -m_use));
+            ls[i] += p0;
+            ls[i + 1] += p1;
+            w[i >> 1] = pack2_bf16(p0, p1);
+          }
+          st_shared_v4(p_s + half * kSub + swz128(q, c), make_uint4(w[0], w[1], w[2], w[3]));
         }
-        st_shared_v4(p_s + half * kSub + swz128(q, c), make_uint4(w[0], w[1], w[2], w[3]));
+        l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
-      l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(smem_u32(&hdr->s_free));
       mbar_arrive(smem_u32(&hdr->p_full));
     }
     if (ok && nt > 0) {
@@ -323,7 +357,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     named_bar(2 + (warp & 3), 64);
     const float l_row = hdr->psum[0][q] + hdr->psum[1][q];
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-    const bool have = ok && nt > 0;
+    const bool have = ok && nt > 0 && live;
     float ov[HO];
     if (have) {  // warp-uniform
 #pragma unroll
@@ -357,7 +391,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     } else {
       // park the unnormalised O row and (m, l) for the cluster merge
-      float* po = reinterpret_cast<float*>(base + (kv_s - base_s));
+      float* po = reinterpret_cast<float*>(base + (k_s - base_s));
       constexpr int PLD = DH + 4;
 #pragma unroll
       for (int i = 0; i < HO; i += 4)
@@ -377,9 +411,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // memory in ascending split order, each weighted by 2^(m_s - M) / L.
     cluster_sync();
     constexpr int PLD = DH + 4;
-    float* po = reinterpret_cast<float*>(base + (kv_s - base_s));
+    float* po = reinterpret_cast<float*>(base + (k_s - base_s));
     float2* mlp = reinterpret_cast<float2*>(po + 128 * PLD);
-    const uint32_t po_u = kv_s, ml_u = smem_u32(mlp);
+    const uint32_t po_u = k_s, ml_u = smem_u32(mlp);
     float* w_loc = reinterpret_cast<float*>(mlp + 128);
     const int S = p.splits;
     const int rank = static_cast<int>(cluster_ctarank());
@@ -442,7 +476,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 

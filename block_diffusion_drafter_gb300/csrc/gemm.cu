@@ -27,8 +27,9 @@ namespace dfl {
 namespace {
 
 constexpr int kSLD = 129;  // staging row stride (floats): conflict-free both ways
+constexpr int kMaxSplitK = 8;  // split-K CTAs per cluster (portable cluster size)
 // barriers + token table, plus slack to align the tile ring to 1024 bytes
-constexpr size_t kSmemHeaderBytes = 3072;
+constexpr size_t kSmemHeaderBytes = 4608;
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
@@ -51,9 +52,9 @@ __device__ __forceinline__ void store_out(void* out, int bf16, size_t idx, float
 constexpr int kEpiBatch = 2;
 
 struct TokInfo {
-  int pos[kBM];     // cache position of the tile's token x, -1 = skip
-  int seq[kBM];     // sequence of token x
-  float rstd[kBM];  // folded RMSNorm scale of token x (1 when not folded)
+  int pos[kBM];       // cache position of the chunk's token x, -1 = skip
+  int seq[kBM];       // sequence of token x
+  float rstd[kMaxBN]; // folded RMSNorm scale of the tile's token x (1 when not folded)
 };
 
 __device__ __forceinline__ float gain_at(const void* g, int bf16, int i) {
@@ -63,25 +64,40 @@ __device__ __forceinline__ float gain_at(const void* g, int bf16, int i) {
 
 // Folded RMSNorm scale 1 / sqrt(mean(h^2) + eps) of tokens tok0 .. tok0+n-1
 // into out[0 .. n), from their per-128-feature partial sums of squares: one
-// warp per token, lane k adds slots k, k+32, ... (fixed order), then a
-// shuffle tree. Tokens past n_tok get 1. Runs on the 128 epilogue threads.
+// thread per token sums its slots in ascending order, eight 16-byte loads in
+// flight at a time (the sums are latency-bound, not bandwidth-bound). Tokens
+// past n_tok get 1. Runs on the 128 epilogue threads.
 __device__ __forceinline__ void folded_rstd(const Epi& e, float* out, int tok0, int n, int etid) {
-  const int w = etid >> 5, lane = etid & 31;
-  for (int t = w; t < n; t += 4) {
+  for (int t = etid; t < n; t += 128) {
     const int tok = tok0 + t;
-    float ss = 0.f;
-    if (tok < e.n_tok)
-      for (int k = lane; k < e.n_ss; k += 32) ss += e.ss_in[static_cast<size_t>(tok) * e.n_ss + k];
+    float r = 1.f;
+    if (tok < e.n_tok) {
+      const float* src = e.ss_in + static_cast<size_t>(tok) * e.n_ss;
+      float ss = 0.f;
+      int k = 0;
+      if ((e.n_ss & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        const int n4 = e.n_ss >> 2;
+        for (int k4 = 0; k4 < n4; k4 += 8) {
+          float4 v[8];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (lane == 0) out[t] = tok < e.n_tok ? 1.0f / sqrtf(ss / static_cast<float>(e.d_model) + e.eps) : 1.f;
+          for (int i = 0; i < 8; ++i) v[i] = k4 + i < n4 ? s4[k4 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss += ((v[i].x + v[i].y) + v[i].z) + v[i].w;
+        }
+        k = e.n_ss;
+      }
+      for (; k < e.n_ss; ++k) ss += src[k];
+      r = 1.0f / sqrtf(ss / static_cast<float>(e.d_model) + e.eps);
+    }
+    out[t] = r;
   }
 }
 
 // Whether the kernel computes the folded-norm scales of the whole tile (one
 // per B row) while the main loop runs, instead of per chunk in the epilogue.
 __device__ __forceinline__ bool rstd_per_tile(const GemmArgs& g) {
-  return g.epi.ss_in != nullptr && g.swap != 0 && g.bn <= kBM;
+  return g.epi.ss_in != nullptr && g.swap != 0 && g.bn <= kMaxBN;
 }
 
 template <int kOp>
@@ -601,7 +617,8 @@ __global__ void __launch_bounds__(kGemmThreads)
     // split order, then runs the epilogue on them. A second barrier keeps
     // every partial alive until all peers have read it: each CTA arrives as
     // soon as its reads are done and waits only at the very end, so the
-    // epilogue runs while slower peers finish reading.
+    // epilogue runs while slower peers finish reading. Remote loads are slow
+    // to return, so each thread requests every split's value before adding.
     cluster_sync();
     if (warp >= 2) {
       const int etid = threadIdx.x - 64;
@@ -616,14 +633,20 @@ __global__ void __launch_bounds__(kGemmThreads)
       for (int cb = c0; cb < c1; cb += kBM) {
         const int cols = min(kBM, c1 - cb);
         if (ok) {
-          for (int it = etid; it < cols * (kBM / 4); it += 128) {
+          const int n_items = cols * (kBM / 4);
+          for (int it = etid; it < n_items; it += 128) {
             const int b = it / (kBM / 4), a = (it % (kBM / 4)) * 4;
             const uint32_t off = static_cast<uint32_t>(((cb + b) * kBM + a) * 4);
+            float4 v[kMaxSplitK];
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplitK; ++sp)
+              if (sp < g.splits) v[sp] = ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(sp)));
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int sp = 0; sp < g.splits; ++sp) {
-              const float4 v = ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(sp)));
-              acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplitK; ++sp) {
+              if (sp < g.splits) {
+                acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w;
+              }
             }
             S[b * kSLD + a] = acc.x;
             S[b * kSLD + a + 1] = acc.y;
@@ -736,7 +759,7 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
     splits = slots / (tiles > 0 ? tiles : 1);
     if (const char* e = getenv("DFLASH_GEMM_SPLITS")) splits = atoi(e);   // tuning override
     if (splits > KT / 4) splits = KT / 4;
-    if (splits > 8) splits = 8;
+    if (splits > kMaxSplitK) splits = kMaxSplitK;
     if (splits < 1) splits = 1;
     // the partial tile and the reduced column slice must fit in the ring
     const size_t ring = static_cast<size_t>(stages) * stage;
@@ -744,7 +767,7 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
       const int per = (p.bn + splits - 1) / splits;
       const size_t need = static_cast<size_t>(p.bn) * kBM * 4 + static_cast<size_t>(per < kBM ? per : kBM) * 129 * 4;
       if (need <= ring) break;
-      if (splits < 8 && splits < KT / 4) ++splits; else { splits = 1; break; }
+      if (splits < kMaxSplitK && splits < KT / 4) ++splits; else { splits = 1; break; }
     }
   }
   p.kt_per_split = (KT + splits - 1) / splits;
