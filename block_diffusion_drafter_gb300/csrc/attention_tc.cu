@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kTileKeys = 128;
 constexpr uint32_t kSub = 128 * 128;     // one 128-row x 128-byte swizzled sub-tile (16 KB)
-constexpr int kMaxCluster = 16;
+constexpr int kMaxCluster = 12;  // split-KV CTAs per cluster (the planner never exceeds it)
 constexpr float kLog2eTc = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.0f;     // log2 units the running max may lag behind
 
@@ -66,6 +66,11 @@ __device__ __forceinline__ float exp2_approx(float x) {
 }
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
 }
 // Bounded wait whose outcome is the same on every lane of the warp (the
 // warp-collective tcgen05 loads that follow need a converged warp).
@@ -408,44 +413,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (p.splits > 1) {
     // Split-KV merge inside the cluster: CTA r merges a slice of the query
     // rows, reading every split's O row and (m, l) through distributed shared
-    // memory in ascending split order, each weighted by 2^(m_s - M) / L.
+    // memory in ascending split order, each weighted by 2^(m_s - M) / L. A
+    // thread requests all of its remote values at once (one round trip), and
+    // arrives on the closing cluster barrier as soon as its reads are done.
     cluster_sync();
     constexpr int PLD = DH + 4;
-    float* po = reinterpret_cast<float*>(base + (k_s - base_s));
-    float2* mlp = reinterpret_cast<float2*>(po + 128 * PLD);
-    const uint32_t po_u = k_s, ml_u = smem_u32(mlp);
-    float* w_loc = reinterpret_cast<float*>(mlp + 128);
+    const uint32_t po_u = k_s, ml_u = k_s + 128 * PLD * 4;
     const int S = p.splits;
     const int rank = static_cast<int>(cluster_ctarank());
     const int per = (n_q + S - 1) / S;
     const int r0 = rank * per, r1 = min(n_q, r0 + per);
     const int nrows = r1 > r0 ? r1 - r0 : 0;
-    float2* mls = reinterpret_cast<float2*>(w_loc + ((per * S + 1) & ~1));
-    for (int pi = threadIdx.x; pi < nrows * S; pi += blockDim.x) {
-      const int qr = r0 + pi / S, s2 = pi % S;
-      float2 v;
-      asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
-                   : "=f"(v.x), "=f"(v.y)
-                   : "r"(mapa_shared(ml_u + qr * 8, s2))
-                   : "memory");
-      mls[pi] = v;
-    }
-    __syncthreads();
-    for (int r = threadIdx.x; r < nrows; r += blockDim.x) {
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < S; ++s2)
-        if (mls[r * S + s2].y > 0.f) M = fmaxf(M, mls[r * S + s2].x);
-      float L = 0.f;
-      for (int s2 = 0; s2 < S; ++s2) {
-        const float2 v = mls[r * S + s2];
-        const float w = v.y > 0.f ? exp2f(v.x - M) : 0.f;
-        w_loc[r * S + s2] = w;
-        L += v.y * w;
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      for (int s2 = 0; s2 < S; ++s2) w_loc[r * S + s2] *= inv;
-    }
-    __syncthreads();
     constexpr int D4 = DH / 4;
     const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -453,14 +431,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int r = it / D4, qr = r0 + r, d = (it % D4) * 4;
       const uint32_t off = po_u + static_cast<uint32_t>((qr * PLD + d) * 4);
       float4 v[kMaxCluster];
+      float2 ml[kMaxCluster];
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxCluster; ++s2) {
+        if (s2 < S) {
+          ml[s2] = ld_dsmem_f2(mapa_shared(ml_u + qr * 8, s2));
+          v[s2] = ld_dsmem_f4(mapa_shared(off, s2));
+        }
+      }
+      float M = -INFINITY;
 #pragma unroll
       for (int s2 = 0; s2 < kMaxCluster; ++s2)
-        if (s2 < S) v[s2] = ld_dsmem_f4(mapa_shared(off, s2));
+        if (s2 < S && ml[s2].y > 0.f) M = fmaxf(M, ml[s2].x);
+      float L = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxCluster; ++s2)
+        if (s2 < S) L += ml[s2].y * (ml[s2].y > 0.f ? exp2f(ml[s2].x - M) : 0.f);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int s2 = 0; s2 < kMaxCluster; ++s2) {
         if (s2 < S) {
-          const float w = w_loc[r * S + s2];
+          const float w = (ml[s2].y > 0.f ? exp2f(ml[s2].x - M) : 0.f) * inv;
           acc.x += v[s2].x * w; acc.y += v[s2].y * w; acc.z += v[s2].z * w; acc.w += v[s2].w * w;
         }
       }
@@ -471,13 +463,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       store_hilo(out, oi + 2, p.out_lo_off, acc.z);
       store_hilo(out, oi + 3, p.out_lo_off, acc.w);
     }
-    cluster_sync();
+    cluster_arrive();
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // the peers may still be reading this CTA's partial rows
+  if (p.splits > 1) cluster_wait();
 }
 
 }  // namespace
