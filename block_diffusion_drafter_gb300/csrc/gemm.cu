@@ -43,13 +43,20 @@ __device__ __forceinline__ void store_out(void* out, int bf16, size_t idx, float
 // Applies the epilogue to one staged chunk: S[b * kSLD + a] holds C for
 // A-row a (0..127) and B-row col0 + b (0 <= b < cols) of tile (m_tile, n_tile).
 // Runs on the 128 epilogue threads (etid 0..127). Every op works in batches
-// of kEpiBatch elements per thread: all global loads of a batch are issued
+// of a few elements per thread: all global loads of a batch are issued
 // before any of its stores, so the loads overlap instead of serialising
-// behind possibly-aliasing stores. The batch stays small: the epilogue runs
-// once per CTA, while other CTAs on the SM stream weights, and fetching its
-// instructions then costs more than the loads it overlaps (a step of the
-// Qwen3-8B-shaped drafter took 34 us longer with batches of 8 than of 2).
-constexpr int kEpiBatch = 2;
+// behind possibly-aliasing stores. Narrow tiles (a few tokens) use batches of
+// 2: larger batches cost registers and code, and a drafting step at batch 1
+// ran slower with them (758 vs 754 us with 4, 799 us with 8). Wide tiles
+// (many tokens per thread) give the ops whose elements each wait on a global
+// load -- the residual, the RoPE tables -- batches of 4 (the ragged batch-16
+// step: 3.03 vs 3.12 ms).
+template <int kOp, bool kWide>
+__host__ __device__ constexpr int epi_batch() {
+  return kWide && (kOp == EPI_QKV || kOp == EPI_KV || kOp == EPI_ADD_F32) ? 4 : 2;
+}
+// Whether an epilogue op has a separate wide-tile instance.
+constexpr bool has_wide(int op) { return op == EPI_QKV || op == EPI_KV || op == EPI_ADD_F32; }
 
 struct TokInfo {
   int pos[kBM];       // cache position of the chunk's token x, -1 = skip
@@ -100,7 +107,7 @@ __device__ __forceinline__ bool rstd_per_tile(const GemmArgs& g) {
   return g.epi.ss_in != nullptr && g.swap != 0 && g.bn <= kMaxBN;
 }
 
-template <int kOp>
+template <int kOp, bool kWide>
 __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, int col0, int cols,
                                int m_tile, int n_tile, int etid) {
   const Epi& e = g.epi;
@@ -152,12 +159,13 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
       const float gx = kOp == EPI_ADD_F32 && e.xg_out != nullptr && m_tile * kBM + etid < e.n_feat
                            ? gain_at(e.xg_gain, e.xg_bf16, m_tile * kBM + etid)
                            : 0.f;
-      for (int base = etid; base < total; base += 128 * kEpiBatch) {
-        float v[kEpiBatch], r[kEpiBatch];
-        size_t o[kEpiBatch];
-        bool ok[kEpiBatch];
+      constexpr int kB = epi_batch<kOp, kWide>();
+      for (int base = etid; base < total; base += 128 * kB) {
+        float v[kB], r[kB];
+        size_t o[kB];
+        bool ok[kB];
 #pragma unroll
-        for (int u = 0; u < kEpiBatch; ++u) {
+        for (int u = 0; u < kB; ++u) {
           const int idx = base + u * 128;
           int a, b;
           if (g.swap) { a = idx & 127; b = idx >> 7; } else { b = idx % cols; a = idx / cols; }
@@ -170,10 +178,10 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
         }
         if (kOp == EPI_ADD_F32) {
 #pragma unroll
-          for (int u = 0; u < kEpiBatch; ++u)
+          for (int u = 0; u < kB; ++u)
             r[u] = ok[u] ? reinterpret_cast<const float*>(e.out)[o[u]] : 0.f;
 #pragma unroll
-          for (int u = 0; u < kEpiBatch; ++u) {
+          for (int u = 0; u < kB; ++u) {
             if (!ok[u]) continue;
             const float hn = r[u] + v[u];
             reinterpret_cast<float*>(e.out)[o[u]] = hn;
@@ -201,7 +209,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           }
         } else {
 #pragma unroll
-          for (int u = 0; u < kEpiBatch; ++u)
+          for (int u = 0; u < kB; ++u)
             if (ok[u]) store_out(e.out, e.out_bf16, o[u], v[u]);
         }
       }
@@ -272,13 +280,14 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
     case EPI_KV: {
       const int Dh = e.head_dim, half = Dh >> 1;
       const int nq = e.n_q_heads * Dh, nk = e.n_kv_heads * Dh;
-      for (int base = etid; base < total; base += 128 * kEpiBatch) {
-        float y[kEpiBatch], cs[kEpiBatch], sn[kEpiBatch];
-        size_t o[kEpiBatch];
-        int kind[kEpiBatch];  // 0 skip, 1 q, 2 k, 3 v
-        int dd[kEpiBatch], pp[kEpiBatch], xx[kEpiBatch];
+      constexpr int kB = epi_batch<kOp, kWide>();
+      for (int base = etid; base < total; base += 128 * kB) {
+        float y[kB], cs[kB], sn[kB];
+        size_t o[kB];
+        int kind[kB];  // 0 skip, 1 q, 2 k, 3 v
+        int dd[kB], pp[kB], xx[kB];
 #pragma unroll
-        for (int u = 0; u < kEpiBatch; ++u) {
+        for (int u = 0; u < kB; ++u) {
           const int idx = base + u * 128;
           int a, b;
           if (g.swap) { a = idx & 127; b = idx >> 7; } else { b = idx % cols; a = idx / cols; }
@@ -327,9 +336,9 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           }
         }
         // table loads of the whole batch first, then the rotations and stores
-        float c[kEpiBatch], sv[kEpiBatch];
+        float c[kB], sv[kB];
 #pragma unroll
-        for (int u = 0; u < kEpiBatch; ++u) {
+        for (int u = 0; u < kB; ++u) {
           c[u] = 1.f;
           sv[u] = 0.f;
           if (kind[u] != 0 && kind[u] != 3 && e.rope_cos != nullptr) {
@@ -340,7 +349,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           }
         }
 #pragma unroll
-        for (int u = 0; u < kEpiBatch; ++u) {
+        for (int u = 0; u < kB; ++u) {
           if (kind[u] == 0) continue;
           float val = y[u];
           if (kind[u] != 3 && e.rope_cos != nullptr)
@@ -411,8 +420,8 @@ static_assert(sizeof(SmemHeader) + 1023 <= kSmemHeaderBytes, "shared-memory head
 
 // One instantiation per (operand type, split activations, epilogue op), so
 // that each launch runs only the code of its own case.
-template <bool kTF32, bool kSplit, int kOp>
-__global__ void __launch_bounds__(kGemmThreads)
+template <bool kTF32, bool kSplit, int kOp, bool kWide>
+__global__ void __launch_bounds__(kGemmThreads, 3)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap a_map,
                    const __grid_constant__ CUtensorMap b_map, const GemmArgs g, int stages) {
   extern __shared__ uint8_t smem_raw[];
@@ -589,7 +598,7 @@ __global__ void __launch_bounds__(kGemmThreads)
           if (b_split)
             for (int j = 0; j < g.b_pack; ++j) S[j * kSLD + row] += S[(g.b_pack + j) * kSLD + row];
           named_bar(1, 128);
-          apply_epilogue<kOp>(g, S, &hdr->tok, c * kBM, cols, m_tile, n_tile, etid);
+          apply_epilogue<kOp, kWide>(g, S, &hdr->tok, c * kBM, cols, m_tile, n_tile, etid);
           named_bar(1, 128);
         }
       } else {
@@ -659,7 +668,7 @@ __global__ void __launch_bounds__(kGemmThreads)
           cluster_arrive();
           arrived = true;
         }
-        if (ok) apply_epilogue<kOp>(g, S, &hdr->tok, cb, cols, m_tile, n_tile, etid);
+        if (ok) apply_epilogue<kOp, kWide>(g, S, &hdr->tok, cb, cols, m_tile, n_tile, etid);
         named_bar(1, 128);
       }
       if (!arrived) cluster_arrive();
@@ -782,18 +791,30 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
 
 using GemmKernel = void (*)(const CUtensorMap, const CUtensorMap, const GemmArgs, int);
 
-template <bool kTF32, bool kSplit, int... kOps>
+// the wide instance of op kOp where it has one, else its narrow instance
+template <bool kTF32, bool kSplit, int kOp, bool kWide>
+constexpr GemmKernel gemm_kernel_of() {
+  if constexpr (kWide && has_wide(kOp)) return &gemm_tc_kernel<kTF32, kSplit, kOp, true>;
+  else return &gemm_tc_kernel<kTF32, kSplit, kOp, false>;
+}
+template <bool kTF32, bool kSplit, bool kWide, int... kOps>
 struct GemmKernelRow {
-  static constexpr GemmKernel fns[sizeof...(kOps)] = {&gemm_tc_kernel<kTF32, kSplit, kOps>...};
+  static constexpr GemmKernel fns[sizeof...(kOps)] = {gemm_kernel_of<kTF32, kSplit, kOps, kWide>()...};
 };
 constexpr int kNumEpiOps = 7;
 static_assert(EPI_FUSE == kNumEpiOps - 1, "one kernel per epilogue op");
-// [tf32 | bf16 | bf16 with split activations][epilogue op]
-const GemmKernel* const kGemmKernels[3] = {
-    GemmKernelRow<true, false, 0, 1, 2, 3, 4, 5, 6>::fns,
-    GemmKernelRow<false, false, 0, 1, 2, 3, 4, 5, 6>::fns,
-    GemmKernelRow<false, true, 0, 1, 2, 3, 4, 5, 6>::fns,
+// [narrow | wide][tf32 | bf16 | bf16 with split activations][epilogue op]
+const GemmKernel* const kGemmKernels[2][3] = {
+    {GemmKernelRow<true, false, false, 0, 1, 2, 3, 4, 5, 6>::fns,
+     GemmKernelRow<false, false, false, 0, 1, 2, 3, 4, 5, 6>::fns,
+     GemmKernelRow<false, true, false, 0, 1, 2, 3, 4, 5, 6>::fns},
+    {GemmKernelRow<true, false, true, 0, 1, 2, 3, 4, 5, 6>::fns,
+     GemmKernelRow<false, false, true, 0, 1, 2, 3, 4, 5, 6>::fns,
+     GemmKernelRow<false, true, true, 0, 1, 2, 3, 4, 5, 6>::fns},
 };
+// Tiles whose epilogue gives every thread many tokens (batches of 4 and more
+// sequences, prefill) take the wide instances.
+bool wide_tile(const GemmArgs& g) { return g.n_rows >= 64; }
 
 cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, const GemmArgs& args,
                         const GemmPlan& plan, cudaStream_t stream, bool pdl) {
@@ -802,11 +823,12 @@ cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, cons
   if (split != (plan.b_split != 0)) return cudaErrorInvalidValue;  // plan sized the other ring
   if (args.epi.op < 0 || args.epi.op >= kNumEpiOps) return cudaErrorInvalidValue;
   const int variant = args.tf32 ? 0 : (split ? 2 : 1);
-  const GemmKernel kern = kGemmKernels[variant][args.epi.op];
-  static bool configured[3][kNumEpiOps][64] = {};
+  const int wide = wide_tile(args) ? 1 : 0;
+  const GemmKernel kern = kGemmKernels[wide][variant][args.epi.op];
+  static bool configured[2][3][kNumEpiOps][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  bool& done = configured[variant][args.epi.op][dev & 63];
+  bool& done = configured[wide][variant][args.epi.op][dev & 63];
   if (!done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
