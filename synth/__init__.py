@@ -90,6 +90,10 @@ WORKLOADS = {
     # for kernel-level profiler captures
     "qwen3_8b_L1_N2048_B1": Workload(
         "qwen3_8b_L1_N2048_B1", n_layers=1, batch=1, ctx=2048, seed=1006, **_QWEN3_8B),
+    # one-layer version of the long-context case, for captures of the
+    # split-KV attention over 32K keys
+    "qwen3_8b_L1_N32768_B1": Workload(
+        "qwen3_8b_L1_N32768_B1", n_layers=1, batch=1, ctx=32768, seed=1007, **_QWEN3_8B),
     # full draft-verify loop: 8 layers, batch 4, context 4096, 256 cycles
     "qwen3_8b_L8_loop_B4": Workload(
         "qwen3_8b_L8_loop_B4", n_layers=8, batch=4, ctx=4096, cycles=256,
