@@ -346,6 +346,24 @@ def kernel_roofline(cyc: DraftCycle, peak_gbs: float, reps: int = 5):
     return out
 
 
+def long_context_attention(dfl, dev, peak_gbs: float, reps: int = 10) -> dict:
+    """The split-KV attention kernel alone over a 32K-key context: one layer of
+    the Qwen3-8B-shaped drafter, launches timed one by one with CUDA events."""
+    wl = synth.WORKLOADS["qwen3_8b_L1_N32768_B1"]
+    cyc = DraftCycle(dfl, wl, dev)
+    for _ in range(3):
+        cyc.step()
+    a = kernel_roofline(cyc, peak_gbs, reps=reps)["attention"]
+    out = {"workload": wl.name, "launches": a["launches_per_step"] * reps,
+           "us_per_launch": round(1e3 * a["ms_per_step"] / a["launches_per_step"], 2),
+           "bytes_per_launch": a["bytes_per_launch"], "achieved_gbs": round(a["achieved_gbs"], 1),
+           "frac_of_hbm": round(a["frac_of_hbm"], 4),
+           "what": "tcgen05 split-KV attention of one layer over 32768 context + 17 block keys"}
+    del cyc
+    torch.cuda.empty_cache()
+    return out
+
+
 class OracleCycle:
     """The CPU oracle running the same drafting cycle (float64 numpy)."""
 
@@ -558,6 +576,8 @@ def run_gpu(args):
             "paged_kv": dict(measure_variant(cyc, cyc.step_paged, min(args.steps, 50), B * gam, hbm),
                              what="greedy cycle over a paged KV cache (128-key pages, scrambled)"),
         }
+        if wl.dtype == "bf16":
+            next_rows["attention_context_32k"] = long_context_attention(dfl, dev, hbm)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:

@@ -35,16 +35,22 @@ constexpr int kMaxCluster = 12;  // split-KV CTAs per cluster (the planner never
 constexpr float kLog2eTc = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.0f;     // log2 units the running max may lag behind
 
+// Softmax warps per TMEM lane quarter: each takes 128 / kParts keys of every
+// S tile (and DH / kParts columns of O). Two, not four: with four the
+// register budget of 18 warps (96 per thread) spills, and the 32K-context
+// attention ran at 0.50 instead of 0.54 of the HBM peak.
+constexpr int kParts = 2;
+constexpr int kAttnThreads = 64 + 128 * kParts;  // TMA warp, MMA warp, softmax warps
+
 struct AttnSmem {
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t q_full, s_full[2], s_free[2], p_full, o_done;
   uint32_t tmem_base;
   int abort_flag;
-  float pmax[2][128];  // per-half row max of the current tile
-  float psum[2][128];  // per-half row sums at the end
+  float pmax[kParts][128];  // per-part row max of the current tile
+  float psum[kParts][128];  // per-part row sums at the end
 };
 
-constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -224,11 +230,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
-    // Warps 2..9: TMEM lane quarter (warp % 4) gives the query row; `half`
-    // picks keys 64*half..+63 of each S tile and columns of O. A quarter
-    // without query rows (all q >= n_q) computes nothing.
+    // Softmax warps: TMEM lane quarter (warp % 4) gives the query row; `part`
+    // picks keys HK*part..+HK-1 of each S tile and columns HO*part..+HO-1 of
+    // O. A quarter without query rows (all q >= n_q) computes nothing.
     const int q = (warp & 3) * 32 + lane;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const bool live = (warp & 3) * 32 < n_q;   // warp-uniform
     const uint32_t t_row = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
@@ -236,9 +242,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q);
     const size_t row_off = (static_cast<size_t>(b) * p.R + iq) * hq_stride + static_cast<size_t>(kvh * G + gq) * DH;
     constexpr int QC = DH / 8;          // 16-byte chunks of one Q row
-    // this thread's half of Q row q into the swizzled K-major tile (rows >= n_q zero)
+    // this thread's part of Q row q into the swizzled K-major tile (rows >= n_q zero)
 #pragma unroll
-    for (int c = half * (QC / 2); c < (half + 1) * (QC / 2); ++c) {
+    for (int c = part * (QC / kParts); c < (part + 1) * (QC / kParts); ++c) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (q < n_q) v = *reinterpret_cast<const uint4*>(qg + row_off + c * 8);
       st_shared_v4(q_s + (c >> 3) * kSub + swz128(q, c & 7), v);
@@ -247,21 +253,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_arrive(smem_u32(&hdr->q_full));
 
     const float scale = rsqrtf(static_cast<float>(DH)) * kLog2eTc;
-    constexpr int HK = kTileKeys / 2;   // keys per half
-    constexpr int HO = DH / 2;          // O columns per half
+    constexpr int HK = kTileKeys / kParts;   // keys per part
+    constexpr int HO = DH / kParts;          // O columns per part
+    constexpr int kBarThreads = 32 * kParts; // the warps of one lane quarter
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < nt; ++t) {
       const int j = t & 1;
       const int kb = k_begin + t * kTileKeys;
       const int nvalid = min(kTileKeys, k_end - kb);
-      const int nv_half = min(HK, max(0, nvalid - half * HK));
+      const int nv_part = min(HK, max(0, nvalid - part * HK));
       if (!warp_wait(smem_u32(&hdr->s_full[j]), (t >> 1) & 1)) { ok = false; break; }
       float sv[HK];
       if (live) {
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < HK; c0 += 16) tmem_ld16(t_row + j * kTileKeys + half * HK + c0, sv + c0);
+        for (int c0 = 0; c0 < HK; c0 += 16) tmem_ld16(t_row + j * kTileKeys + part * HK + c0, sv + c0);
         tmem_ld_wait();
       }
       // S_t is in registers: its buffer may take S_{t+2}
@@ -271,10 +278,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool rescale = false;
       float m_new = m_run;
       if (live) {
-        if (nv_half < HK) {
+        if (nv_part < HK) {
 #pragma unroll
           for (int i = 0; i < HK; ++i)
-            if (i >= nv_half) sv[i] = -INFINITY;
+            if (i >= nv_part) sv[i] = -INFINITY;
         }
         float m8[8];
 #pragma unroll
@@ -283,10 +290,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int i = 8; i < HK; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
         float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                          fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        // both halves of the row agree on its max
-        hdr->pmax[half][q] = mx;
-        named_bar(2 + (warp & 3), 64);
-        mx = fmaxf(hdr->pmax[0][q], hdr->pmax[1][q]) * scale;
+        // all parts of the row agree on its max
+        hdr->pmax[part][q] = mx;
+        named_bar(2 + (warp & 3), kBarThreads);
+        mx = hdr->pmax[0][q];
+#pragma unroll
+        for (int k = 1; k < kParts; ++k) mx = fmaxf(mx, hdr->pmax[k][q]);
+        mx *= scale;
         m_new = fmaxf(m_run, mx);
         rescale = (m_run == -INFINITY) || (m_new > m_run + kLazyRescale);
         m_use = rescale ? m_new : m_run;
@@ -302,12 +312,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (rescale) l_run *= alpha;
           float ov[HO];
 #pragma unroll
-          for (int c0 = 0; c0 < HO; c0 += 16) tmem_ld16(t_row + kOCol + half * HO + c0, ov + c0);
+          for (int c0 = 0; c0 < HO; c0 += 16) tmem_ld16(t_row + kOCol + part * HO + c0, ov + c0);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < HO; ++i) ov[i] *= alpha;
 #pragma unroll
-          for (int c0 = 0; c0 < HO; c0 += 16) tmem_st16(t_row + kOCol + half * HO + c0, ov + c0);
+          for (int c0 = 0; c0 < HO; c0 += 16) tmem_st16(t_row + kOCol + part * HO + c0, ov + c0);
           tmem_st_wait();
         }
       }
@@ -321,12 +331,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < NSUB; ++jj)
 #pragma unroll
-            for (int c = half * 4; c < half * 4 + 4; ++c)
+            for (int c = part * (8 / kParts); c < (part + 1) * (8 / kParts); ++c)
               st_shared_v4(vt + jj * kSub + q * 128 + c * 16, make_uint4(0u, 0u, 0u, 0u));
         }
       }
       if (live) {
-        // P = 2^(s * scale - m) as bf16 into sub-tile `half` of the K-major P tile
+        // P = 2^(s * scale - m) as bf16 into the K-major P tile (keys HK*part..)
         float ls[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) ls[i] = 0.f;
@@ -341,7 +351,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ls[i + 1] += p1;
             w[i >> 1] = pack2_bf16(p0, p1);
           }
-          st_shared_v4(p_s + half * kSub + swz128(q, c), make_uint4(w[0], w[1], w[2], w[3]));
+          const int key = part * HK + c * 8;
+          st_shared_v4(p_s + (key >> 6) * kSub + swz128(q, (key & 63) >> 3), make_uint4(w[0], w[1], w[2], w[3]));
         }
         l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
@@ -357,16 +368,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       report(p.dev_status, DFLASH_ERR_TIMEOUT);
       atomicExch(&hdr->abort_flag, 1);
     }
-    // row sum over both halves (same running max), in a fixed order
-    hdr->psum[half][q] = l_run;
-    named_bar(2 + (warp & 3), 64);
-    const float l_row = hdr->psum[0][q] + hdr->psum[1][q];
+    // row sum over the parts (same running max), in a fixed order
+    hdr->psum[part][q] = l_run;
+    named_bar(2 + (warp & 3), kBarThreads);
+    float l_row = hdr->psum[0][q];
+#pragma unroll
+    for (int k = 1; k < kParts; ++k) l_row += hdr->psum[k][q];
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     const bool have = ok && nt > 0 && live;
     float ov[HO];
     if (have) {  // warp-uniform
 #pragma unroll
-      for (int c0 = 0; c0 < HO; c0 += 16) tmem_ld16(t_row + kOCol + half * HO + c0, ov + c0);
+      for (int c0 = 0; c0 < HO; c0 += 16) tmem_ld16(t_row + kOCol + part * HO + c0, ov + c0);
       tmem_ld_wait();
     }
     if (p.splits == 1) {
@@ -380,7 +393,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint4 w;
           w.x = pack2_bf16(x[0], x[1]); w.y = pack2_bf16(x[2], x[3]);
           w.z = pack2_bf16(x[4], x[5]); w.w = pack2_bf16(x[6], x[7]);
-          *reinterpret_cast<uint4*>(out + row_off + half * HO + c0) = w;
+          *reinterpret_cast<uint4*>(out + row_off + part * HO + c0) = w;
           if (p.out_lo_off) {
             const __nv_bfloat162* hw = reinterpret_cast<const __nv_bfloat162*>(&w);
             uint4 lw;
@@ -390,7 +403,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               const float2 hf = __bfloat1622float2(hw[i]);
               l[i] = pack2_bf16(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
             }
-            *reinterpret_cast<uint4*>(out + p.out_lo_off + row_off + half * HO + c0) = lw;
+            *reinterpret_cast<uint4*>(out + p.out_lo_off + row_off + part * HO + c0) = lw;
           }
         }
       }
@@ -400,9 +413,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       constexpr int PLD = DH + 4;
 #pragma unroll
       for (int i = 0; i < HO; i += 4)
-        *reinterpret_cast<float4*>(&po[q * PLD + half * HO + i]) =
+        *reinterpret_cast<float4*>(&po[q * PLD + part * HO + i]) =
             have ? make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
-      if (half == 0) {
+      if (part == 0) {
         float2* ml = reinterpret_cast<float2*>(po + 128 * PLD);
         ml[q] = have ? make_float2(m_run, l_row) : make_float2(-INFINITY, 0.f);
       }
