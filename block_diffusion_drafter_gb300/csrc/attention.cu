@@ -92,29 +92,40 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
 }  // namespace
 
 void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
-                    int* chunk) {
+                    int* chunk, int* merge_global) {
   const int n_keys = (max_ctx < ncap ? max_ctx : ncap) + R;
   const int per_seq = B * Hkv > 0 ? B * Hkv : 1;
-  int target = (2 * 152 + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
-  if (target > kMaxAttnCluster) target = kMaxAttnCluster;
-  // whole 128-key tiles per split (the tcgen05 kernel's tile)
-  int c = (n_keys + target - 1) / target;
-  c = (c + 127) / 128 * 128;
-  if (c < 128) c = 128;
-  int sp = (n_keys + c - 1) / c;
-  while (sp > kMaxAttnCluster) {
-    c += 128;
-    sp = (n_keys + c - 1) / c;
-  }
+  const int tiles = (n_keys + 127) / 128;
+  // Long contexts with few (sequence, KV head) pairs: a cluster of at most
+  // kMaxAttnCluster splits per pair would leave SMs idle, so take one split
+  // per SM (each at least two 128-key tiles) and merge through the workspace.
+  int wide = 152 / per_seq;
+  if (wide > kAttnMaxSlots / per_seq) wide = kAttnMaxSlots / per_seq;
+  if (wide > tiles / 2) wide = tiles / 2;
+  int sp, c;
+  bool global = wide > kMaxAttnCluster;
   if (const char* e = getenv("DFLASH_ATTN_SPLITS")) {   // tuning override
     sp = atoi(e);
     if (sp < 1) sp = 1;
+    if (sp > kAttnMaxSlots / per_seq) sp = kAttnMaxSlots / per_seq < 1 ? 1 : kAttnMaxSlots / per_seq;
+    global = sp > kMaxAttnCluster;
+  } else if (global) {
+    sp = wide;
+  } else {
+    sp = (2 * 152 + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
     if (sp > kMaxAttnCluster) sp = kMaxAttnCluster;
-    c = ((n_keys + sp - 1) / sp + 127) / 128 * 128;
+  }
+  // whole 128-key tiles per split (the tcgen05 kernel's tile)
+  c = ((n_keys + sp - 1) / sp + 127) / 128 * 128;
+  if (c < 128) c = 128;
+  sp = (n_keys + c - 1) / c;
+  while (!global && sp > kMaxAttnCluster) {
+    c += 128;
     sp = (n_keys + c - 1) / c;
   }
   *splits = sp < 1 ? 1 : sp;
   *chunk = c;
+  *merge_global = (global && *splits > 1) ? 1 : 0;
   (void)Hq;
   (void)Dh;
 }

@@ -20,7 +20,10 @@
 // (lane 0 K, lane 1 V), warp 1 the MMAs, warps 2-9 run the softmax (two per
 // TMEM lane quarter); a quarter holding no query row only keeps the barrier
 // counts. The key slices of one (sequence, KV head) form a thread-block
-// cluster whose partial results are merged through distributed shared memory.
+// cluster whose partial results are merged through distributed shared memory;
+// for long contexts with few (sequence, KV head) pairs there are more slices
+// than a cluster holds (one per SM), and attn_merge_kernel merges them from
+// the workspace.
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -73,6 +76,21 @@ __device__ __forceinline__ float exp2_approx(float x) {
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
+// L2 prefetch of one TMA box (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+#ifndef DFLASH_ATTN_L2_AHEAD
+#define DFLASH_ATTN_L2_AHEAD 0
+#endif
+// Tiles a K or V producer keeps requested ahead into L2 beyond its 2-stage
+// ring: the ring alone holds too few bytes in flight per SM for the HBM
+// latency under load.
+constexpr int kL2Ahead = DFLASH_ATTN_L2_AHEAD;
+
 __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
@@ -154,8 +172,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const CUtensorMap* map = is_v ? &v_map : &k_map;
       const uint32_t ring = is_v ? v_s : k_s;
       const uint64_t pol = l2_evict_first();
+      // box coordinates of tile t: (y, z) of the contiguous cache slab or of its page
+      auto coords = [&](int t, int& y, int& z) -> bool {
+        const int kb = k_begin + t * kTileKeys;
+        z = slab;
+        y = kb;
+        if (p.page_table != nullptr) {
+          const int pg = p.page_table[static_cast<size_t>(b) * p.pages_per_seq + kb / kPageKeys];
+          if (pg < 0 || pg >= p.n_pages) return false;
+          z = (p.layer * p.n_pages + pg) * p.n_kv_heads + kvh;
+          y = 0;
+        }
+        return true;
+      };
+      auto prefetch = [&](int t) {
+        int y, z;
+        if (kL2Ahead > 2 && t < nt && coords(t, y, z)) {
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j) tma_prefetch_l2_3d(map, 64 * j, y, z);
+        }
+      };
+      for (int t = 2; t < kL2Ahead; ++t) prefetch(t);
       for (int t = 0; t < nt; ++t) {
         const int st = t & 1, u = t >> 1;
+        prefetch(t + kL2Ahead);
         const uint32_t empty = smem_u32(is_v ? &hdr->v_empty[st] : &hdr->k_empty[st]);
         if (u > 0 && !mbar_wait(empty, (u - 1) & 1)) {
           report(p.dev_status, DFLASH_ERR_TIMEOUT);
@@ -165,15 +205,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (*abort_flag) break;
         const uint32_t bar = smem_u32(is_v ? &hdr->v_full[st] : &hdr->k_full[st]);
         const uint32_t dst = ring + st * kTileBytes;
-        const int kb = k_begin + t * kTileKeys;
-        int z = slab, y = kb;
-        if (p.page_table != nullptr) {  // the tile is one page of the pool
-          int pg = p.page_table[static_cast<size_t>(b) * p.pages_per_seq + kb / kPageKeys];
-          if (pg < 0 || pg >= p.n_pages) {
-            report(p.dev_status, DFLASH_ERR_CAPACITY);
-            pg = 0;
-          }
-          z = (p.layer * p.n_pages + pg) * p.n_kv_heads + kvh;
+        int y, z;
+        if (!coords(t, y, z)) {  // the tile is a page outside the pool
+          report(p.dev_status, DFLASH_ERR_CAPACITY);
+          z = p.layer * p.n_pages * p.n_kv_heads + kvh;   // page 0
           y = 0;
         }
         mbar_expect_tx(bar, kTileBytes);
@@ -407,6 +442,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       }
+    } else if (p.merge_global) {
+      // this split's unnormalised O row and (m, l) to its workspace slot
+      if (q < n_q) {
+        float* slot = p.partials + (static_cast<size_t>(b * p.n_kv_heads + kvh) * p.splits + sp) *
+                                       attn_slot_floats(DH);
+        float4* orow = reinterpret_cast<float4*>(slot + static_cast<size_t>(q) * DH + part * HO);
+#pragma unroll
+        for (int i = 0; i < HO; i += 4)
+          orow[i / 4] = have ? make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (part == 0)
+          reinterpret_cast<float2*>(slot + static_cast<size_t>(128) * DH)[q] =
+              have ? make_float2(m_run, l_row) : make_float2(-INFINITY, 0.f);
+      }
     } else {
       // park the unnormalised O row and (m, l) for the cluster merge
       float* po = reinterpret_cast<float*>(base + (k_s - base_s));
@@ -423,7 +471,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_before();
   }
 
-  if (p.splits > 1) {
+  if (p.splits > 1 && !p.merge_global) {
     // Split-KV merge inside the cluster: CTA r merges a slice of the query
     // rows, reading every split's O row and (m, l) through distributed shared
     // memory in ascending split order, each weighted by 2^(m_s - M) / L. A
@@ -484,7 +532,102 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   // the peers may still be reading this CTA's partial rows
-  if (p.splits > 1) cluster_wait();
+  if (p.splits > 1 && !p.merge_global) cluster_wait();
+}
+
+// Merge of the split partials written to the workspace: CTA (x, kvh, b)
+// takes query rows 4x..4x+3 of one (sequence, KV head), a warp per row, each
+// lane DH/32 of its columns. Lane s holds split s's (m, l) (s, s+32, ... for
+// more splits); the running max M is a warp reduction, the weights
+// 2^(m_s - M) / L and the column sums are taken in ascending split order, the
+// same arithmetic as the cluster merge. The O rows of the first kMergeBatch
+// splits are requested together with the (m, l) pairs, so a row costs one L2
+// round trip for up to kMergeBatch splits.
+constexpr int kMergeBatch = 24;
+template <int DH>
+__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int DPT = DH / 32;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.n_q_heads / p.n_kv_heads;
+  const int n_q = G * p.R;
+  const int qr = blockIdx.x * 4 + static_cast<int>(threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (qr >= n_q) return;   // warp-uniform: whole warps leave
+  const int S = p.splits;
+  const size_t slot_f = attn_slot_floats(DH);
+  const float* base = p.partials + static_cast<size_t>(b * p.n_kv_heads + kvh) * S * slot_f;
+  const float2* ml = reinterpret_cast<const float2*>(base + static_cast<size_t>(128) * DH) + qr;
+  const float* row = base + static_cast<size_t>(qr) * DH + lane * DPT;
+  auto load_o = [&](int s2, float* x) {
+    if (DPT == 4) {
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(row + s2 * slot_f));
+      x[0] = t.x; x[1 % DPT] = t.y; x[2 % DPT] = t.z; x[3 % DPT] = t.w;
+    } else {
+      const float2 t = __ldcg(reinterpret_cast<const float2*>(row + s2 * slot_f));
+      x[0] = t.x; x[1 % DPT] = t.y;
+    }
+  };
+  float x[kMergeBatch][DPT];
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u)
+    if (u < S) load_o(u, x[u]);
+  // (m, l) of splits lane, lane + 32, ... (at most kAttnMaxSlots splits)
+  constexpr int kPer = (kAttnMaxSlots + 31) / 32;
+  float2 mv[kPer];
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int s2 = lane + 32 * k;
+    mv[k] = s2 < S ? __ldcg(ml + s2 * (slot_f / 2)) : make_float2(-INFINITY, 0.f);
+    if (mv[k].y > 0.f) M = fmaxf(M, mv[k].x);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float wk[kPer];   // 2^(m_s - M) of this lane's splits
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) wk[k] = mv[k].y > 0.f ? exp2f(mv[k].x - M) : 0.f;
+  // split s2's weight and l, broadcast from the lane that holds it
+  auto from_lane = [&](const float* v, int s2) {
+    float r = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const float t = __shfl_sync(0xffffffffu, v[k], s2 & 31);
+      if ((s2 >> 5) == k) r = t;
+    }
+    return r;
+  };
+  float lk[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) lk[k] = mv[k].y;
+  float L = 0.f;
+  for (int s2 = 0; s2 < S; ++s2) L += from_lane(lk, s2) * from_lane(wk, s2);   // ascending order
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float acc[DPT];
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) acc[i] = 0.f;
+  for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u)
+        if (s0 + u < S) load_o(s0 + u, x[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float w = from_lane(wk, s0 + u) * inv;
+      if (s0 + u < S) {
+#pragma unroll
+        for (int i = 0; i < DPT; ++i) acc[i] += x[u][i] * w;
+      }
+    }
+  }
+  const int g = qr / p.R, i = qr % p.R;
+  const size_t hq_stride = static_cast<size_t>(p.n_q_heads) * DH;
+  const size_t oi = (static_cast<size_t>(b) * p.R + i) * hq_stride + static_cast<size_t>(kvh * G + g) * DH + lane * DPT;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+  for (int k = 0; k < DPT; ++k) store_hilo(out, oi + k, p.out_lo_off, acc[k]);
 }
 
 }  // namespace
@@ -494,7 +637,11 @@ namespace dfl {
 
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl) {
   if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
-  if ((a.n_q_heads / a.n_kv_heads) * a.R > 128 || a.splits > kMaxCluster) return cudaErrorInvalidValue;
+  if ((a.n_q_heads / a.n_kv_heads) * a.R > 128) return cudaErrorInvalidValue;
+  const bool global = a.splits > 1 && a.merge_global;
+  if (!global && a.splits > kMaxCluster) return cudaErrorInvalidValue;
+  if (global && (a.partials == nullptr || a.B * a.n_kv_heads * a.splits > kAttnMaxSlots))
+    return cudaErrorInvalidValue;
   // one tensor map per cache over all layers: [L * max_batch * Hkv][Ncap][Dh],
   // or for page pools [L * n_pages * Hkv][kPageKeys][Dh] (a tile is a page)
   CUtensorMap km, vm;
@@ -531,7 +678,7 @@ cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
-  if (a.splits > 1) {
+  if (a.splits > 1 && !global) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = a.splits;
     attr[n].val.clusterDim.y = 1;
@@ -541,6 +688,24 @@ cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl
   cfg.attrs = n ? attr : nullptr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, km, vm, a);
+}
+
+cudaError_t launch_attention_merge(const AttnArgs& a, cudaStream_t stream, bool pdl) {
+  if (!(a.bf16 && a.splits > 1 && a.merge_global)) return cudaSuccess;
+  if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
+  // merge of the workspace partials: 4 query rows per CTA
+  cudaLaunchConfig_t mc = {};
+  const int n_q = (a.n_q_heads / a.n_kv_heads) * a.R;
+  mc.gridDim = dim3((n_q + 3) / 4, a.n_kv_heads, a.B);
+  mc.blockDim = dim3(128, 1, 1);
+  mc.stream = stream;
+  cudaLaunchAttribute mattr[1];
+  mattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  mattr[0].val.programmaticStreamSerializationAllowed = 1;
+  mc.attrs = pdl ? mattr : nullptr;
+  mc.numAttrs = pdl ? 1 : 0;
+  return a.head_dim == 128 ? cudaLaunchKernelEx(&mc, attn_merge_kernel<128>, a)
+                           : cudaLaunchKernelEx(&mc, attn_merge_kernel<64>, a);
 }
 
 }  // namespace dfl

@@ -18,7 +18,7 @@ inline int elem_bytes(const dflash_config* c) { return c->dtype == DFLASH_BF16 ?
 inline int rows_per_block(const dflash_config* c) { return c->gamma + 1; }
 
 struct WsLayout {
-  size_t h, xn, q, attn_o, act, z, ss, lm_keys, v_keys, v_count, samp;
+  size_t h, xn, q, attn_o, act, z, ss, lm_keys, v_keys, v_count, samp, attn_part;
   size_t row_ss;
   size_t fixed;  // bytes before row_ss
 };
@@ -45,6 +45,10 @@ WsLayout ws_layout(const dflash_config* c) {
   L.v_keys = take(rows * 8);
   L.v_count = take(static_cast<size_t>(c->max_batch) * 4);
   L.samp = take(dfl::sample_ws_bytes(c->max_batch, c->gamma, c->vocab));
+  // split-KV partials of long contexts (tcgen05 attention, bf16 drafters)
+  L.attn_part = take(c->dtype == DFLASH_BF16
+                         ? static_cast<size_t>(dfl::kAttnMaxSlots) * dfl::attn_slot_floats(c->head_dim) * 4
+                         : 0);
   L.row_ss = off;
   L.fixed = off;
   return L;
@@ -620,9 +624,9 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
       launch_copy_f32(layer_dump_opt, h, static_cast<size_t>(rows) * D, cx.s, cx.pdl) != cudaSuccess)
     return DFLASH_ERR_CUDA;
 
-  int a_splits = 1, a_chunk = 0;
+  int a_splits = 1, a_chunk = 0, a_global = 0;
   plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, ncap,
-                 &a_splits, &a_chunk);
+                 &a_splits, &a_chunk, &a_global);
 
   for (int l = 0; l < Lyr; ++l) {
     // Q/K/V projection of RMSNorm(h): RoPE; block K/V into the cache scratch rows
@@ -668,12 +672,20 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
         a.pages_per_seq = pages->pages_per_seq;
       }
       a.splits = a_splits; a.chunk = a_chunk; a.bf16 = bf16;
+      a.merge_global = a_global;
+      a.partials = at<float>(cx.ws, cx.L.attn_part);
       const double kvb = 2.0 * B * c->n_kv_heads * static_cast<double>(max_ctx_hint + R) * c->head_dim * es;
       const double fl = 4.0 * B * c->n_q_heads * R * static_cast<double>(max_ctx_hint + R) * c->head_dim;
       cx.tr.before(DFLASH_K_ATTN, kvb + 2.0 * rows * HD * es, fl);
       st = fail(launch_attention(a, cx.s, cx.pdl));
       cx.tr.after();
       if (st != DFLASH_OK) return st;
+      if (bf16 && a.splits > 1 && a.merge_global) {   // its merge: time, no algorithmic bytes
+        cx.tr.before(DFLASH_K_ATTN, 0.0, 0.0);
+        st = fail(launch_attention_merge(a, cx.s, cx.pdl));
+        cx.tr.after();
+        if (st != DFLASH_OK) return st;
+      }
     }
     // output projection + residual; emits g_ffn (.) h and sums of squares
     {

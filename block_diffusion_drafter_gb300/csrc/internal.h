@@ -138,17 +138,30 @@ struct AttnArgs {
   size_t out_lo_off;      // > 0: bf16 lo = bf16(o - hi) at out + out_lo_off elements
   int* dev_status;
   int B, R, n_q_heads, n_kv_heads, head_dim, ncap, max_batch;
-  int splits, chunk;      // keys per split (multiple of 64); last split takes the rest;
-                          // the splits of one (sequence, KV head) form one cluster
+  int splits, chunk;      // keys per split (multiple of 128); last split takes the rest
+  int merge_global;       // 0: the splits of one (sequence, KV head) form one cluster and merge
+                          //    through distributed shared memory;
+                          // 1: more splits than a cluster holds: each writes its partial rows
+                          //    to `partials` and a second kernel merges them
+  float* partials;        // merge_global: [B][Hkv][splits] slots of attn_slot_floats(head_dim)
   int bf16;
   const int32_t* page_table;   // NULL, or paged caches as in Epi
   int n_pages, pages_per_seq;
 };
+// Floats of one split's partial result: 128 unnormalised O rows of head_dim,
+// then (running max, row sum) of each row.
+__host__ __device__ constexpr size_t attn_slot_floats(int head_dim) {
+  return static_cast<size_t>(128) * head_dim + 256;
+}
+// Partial-result slots in a workspace: B * Hkv * splits on the merge_global path.
+constexpr int kAttnMaxSlots = 160;
 void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
-                    int* chunk);
+                    int* chunk, int* merge_global);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
 // bf16 path on tcgen05 (attention_tc.cu)
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl);
+// Second kernel of the merge_global path (a no-op launch otherwise).
+cudaError_t launch_attention_merge(const AttnArgs& a, cudaStream_t stream, bool pdl);
 
 // Small row kernels.
 // h[b*R + i] = embed[id] (id = ids[b*R + i] when ids is given, else anchor[b]

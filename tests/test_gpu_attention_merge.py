@@ -1,0 +1,64 @@
+"""GPU: the two split-KV merges of the tcgen05 attention agree bit for bit.
+
+Long contexts with few (sequence, KV head) pairs take one split per SM and
+merge the partial rows from the workspace in a second kernel; shorter ones
+merge inside a thread-block cluster. Both combine the same per-split partials
+with the same weights in the same order, so drafts, logits and every layer's
+hidden state must be identical. The workspace path is forced on small shapes
+through the planner's split override (more splits than a cluster holds)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import harness as H
+from tests.test_gpu_paged import fused_context
+
+pytestmark = pytest.mark.gpu
+
+WL64 = synth.Workload("small_bf16_L2_dh64", n_layers=2, d_target=128, n_taps=5, d_model=256,
+                      n_q_heads=8, n_kv_heads=2, head_dim=64, d_ffn=384, vocab=1003, gamma=16,
+                      dtype="bf16", batch=3, ctx=900, seed=19)
+WL128 = WL64.replace(name="small_bf16_L2_dh128", head_dim=128, seed=23)
+
+
+@pytest.fixture(scope="module")
+def dfl(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    return lib
+
+
+def run(dfl, wl, lens, splits):
+    gd = H.GpuDrafter(dfl, wl, max_rows=max(sum(lens), 16), ctx_capacity=1024)
+    gd.inject(fused_context(gd, lens), lens)
+    old = os.environ.get("DFLASH_ATTN_SPLITS")
+    if splits is None:
+        os.environ.pop("DFLASH_ATTN_SPLITS", None)
+    else:
+        os.environ["DFLASH_ATTN_SPLITS"] = str(splits)
+    try:
+        draft, logits, dump = gd.draft(synth.anchors(wl), max(lens), want_logits=True, want_dump=True)
+        torch.cuda.synchronize()
+        gd.check_status()
+    finally:
+        if old is None:
+            os.environ.pop("DFLASH_ATTN_SPLITS", None)
+        else:
+            os.environ["DFLASH_ATTN_SPLITS"] = old
+    return draft, logits, dump
+
+
+@pytest.mark.parametrize("wl", [WL64, WL128], ids=["dh64", "dh128"])
+def test_workspace_merge_equals_cluster_merge(dfl, wl):
+    lens = [900, 250, 0]          # several tiles, a short sequence, an empty context
+    # both plan 128-key splits, 8 of them over the longest context: asked for 8
+    # (a cluster holds them) or for 16 (more than a cluster holds: workspace merge)
+    d_c, l_c, h_c = run(dfl, wl, lens, 8)
+    d_g, l_g, h_g = run(dfl, wl, lens, 16)
+    assert torch.equal(h_g, h_c)
+    assert torch.equal(l_g, l_c)
+    assert torch.equal(d_g, d_c)
+    assert np.isfinite(l_g.cpu().numpy()).all()
