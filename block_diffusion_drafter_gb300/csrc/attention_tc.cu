@@ -588,13 +588,16 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs p) {
   float wk[kPer];   // 2^(m_s - M) of this lane's splits
 #pragma unroll
   for (int k = 0; k < kPer; ++k) wk[k] = mv[k].y > 0.f ? exp2f(mv[k].x - M) : 0.f;
-  // split s2's weight and l, broadcast from the lane that holds it
+  // split s2's weight and l, broadcast from the lane that holds it (one
+  // shuffle while the splits fit in a warp's lanes)
   auto from_lane = [&](const float* v, int s2) {
-    float r = 0.f;
+    float r = __shfl_sync(0xffffffffu, v[0], s2 & 31);
+    if (S > 32) {   // warp-uniform
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const float t = __shfl_sync(0xffffffffu, v[k], s2 & 31);
-      if ((s2 >> 5) == k) r = t;
+      for (int k = 1; k < kPer; ++k) {
+        const float t = __shfl_sync(0xffffffffu, v[k], s2 & 31);
+        if ((s2 >> 5) == k) r = t;
+      }
     }
     return r;
   };
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs p) {
 #pragma unroll
   for (int k = 0; k < kPer; ++k) lk[k] = mv[k].y;
   float L = 0.f;
-  for (int s2 = 0; s2 < S; ++s2) L += from_lane(lk, s2) * from_lane(wk, s2);   // ascending order
+  for (int s2 = 0; s2 < S; ++s2) L = fmaf(from_lane(lk, s2), from_lane(wk, s2), L);   // ascending order
   const float inv = L > 0.f ? 1.f / L : 0.f;
   float acc[DPT];
 #pragma unroll
