@@ -158,15 +158,25 @@ class DraftCycle:
                              self.ctx_len, self.k_cache, self.v_cache, self.status, self.ws)
         del h
         self.ctx0 = self.ctx_len.clone()
-        # per-step inputs
-        self.step_taps = synth.taps(wl, B * R, "step", device)
+        # per-step inputs (anchors, then the tapped states 256 bytes in) and
+        # outputs (drafts, acceptance lengths, committed tokens), each packed
+        # in one device buffer, so that an end-to-end step moves each
+        # direction with one copy
+        taps = synth.taps(wl, B * R, "step", device)
+        a_bytes = (4 * B + 255) // 256 * 256
+        self.io_in = torch.zeros(a_bytes + taps.numel() * taps.element_size(), dtype=torch.uint8, device=device)
+        self.anchor = self.io_in[: 4 * B].view(torch.int32)
+        self.anchor.copy_(torch.as_tensor(synth.anchors(wl), device=device))
+        self.step_taps = self.io_in[a_bytes:].view(taps.dtype).view(taps.shape)
+        self.step_taps.copy_(taps)
+        del taps
         self.h_new = torch.empty((B, R, wl.d_model), dtype=dt, device=device)
         self.n_new = torch.full((B,), R, dtype=torch.int32, device=device)
-        self.anchor = torch.as_tensor(synth.anchors(wl), device=device)
         self.target = synth.target_logits(wl, "step", device, torch.float32)
-        self.draft = torch.empty((B, wl.gamma), dtype=torch.int32, device=device)
-        self.tau = torch.empty(B, dtype=torch.int32, device=device)
-        self.committed = torch.empty((B, R), dtype=torch.int32, device=device)
+        self.io_out = torch.zeros(B * wl.gamma + B + B * R, dtype=torch.int32, device=device)
+        self.draft = self.io_out[: B * wl.gamma].view(B, wl.gamma)
+        self.tau = self.io_out[B * wl.gamma: B * wl.gamma + B]
+        self.committed = self.io_out[B * wl.gamma + B:].view(B, R)
         self.next_anchor = torch.empty(B, dtype=torch.int32, device=device)
         self.max_ctx = int(synth.ctx_lengths(wl).max())
         torch.cuda.synchronize()
@@ -528,12 +538,9 @@ def run_gpu(args):
     value = job_throughput(world, tokens, args.steps, ms)
 
     # end to end through host buffers: inputs H2D from pinned memory, results D2H
-    h_taps = cyc.step_taps.cpu().pin_memory()
+    h_in = cyc.io_in.cpu().pin_memory()          # anchors + tapped states
     h_target = cyc.target.cpu().pin_memory()
-    h_anchor = cyc.anchor.cpu().pin_memory()
-    o_draft = torch.empty_like(cyc.draft, device="cpu").pin_memory()
-    o_tau = torch.empty_like(cyc.tau, device="cpu").pin_memory()
-    o_comm = torch.empty_like(cyc.committed, device="cpu").pin_memory()
+    o_out = torch.empty_like(cyc.io_out, device="cpu").pin_memory()   # drafts, tau, committed
 
     def e2e_body():
         # the step's target logits are needed only by verification: their H2D
@@ -542,14 +549,11 @@ def run_gpu(args):
         copy_stream.wait_stream(cur)
         with torch.cuda.stream(copy_stream):
             cyc.target.copy_(h_target, non_blocking=True)
-        cyc.step_taps.copy_(h_taps, non_blocking=True)
-        cyc.anchor.copy_(h_anchor, non_blocking=True)
+        cyc.io_in.copy_(h_in, non_blocking=True)
         cyc.step_draft()
         cur.wait_stream(copy_stream)
         cyc.step_verify()
-        o_draft.copy_(cyc.draft, non_blocking=True)
-        o_tau.copy_(cyc.tau, non_blocking=True)
-        o_comm.copy_(cyc.committed, non_blocking=True)
+        o_out.copy_(cyc.io_out, non_blocking=True)
 
     copy_stream = torch.cuda.Stream()
     e2e_step = e2e_body
@@ -569,8 +573,8 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     ms_e2e = max_over_ranks(time_steps(e2e_step, args.steps, stream), world, dev)
-    h2d = h_taps.numel() * h_taps.element_size() + h_target.numel() * 4 + h_anchor.numel() * 4
-    d2h = (o_draft.numel() + o_tau.numel() + o_comm.numel()) * 4
+    h2d = h_in.numel() + h_target.numel() * 4
+    d2h = o_out.numel() * 4
 
     launches = cyc.launches_per_step()
     kern = kernel_roofline(cyc, hbm)
