@@ -76,21 +76,6 @@ __device__ __forceinline__ float exp2_approx(float x) {
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
-// L2 prefetch of one TMA box (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-#ifndef DFLASH_ATTN_L2_AHEAD
-#define DFLASH_ATTN_L2_AHEAD 0
-#endif
-// Tiles a K or V producer keeps requested ahead into L2 beyond its 2-stage
-// ring: the ring alone holds too few bytes in flight per SM for the HBM
-// latency under load.
-constexpr int kL2Ahead = DFLASH_ATTN_L2_AHEAD;
-
 __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
@@ -185,17 +170,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         return true;
       };
-      auto prefetch = [&](int t) {
-        int y, z;
-        if (kL2Ahead > 2 && t < nt && coords(t, y, z)) {
-#pragma unroll
-          for (int j = 0; j < NSUB; ++j) tma_prefetch_l2_3d(map, 64 * j, y, z);
-        }
-      };
-      for (int t = 2; t < kL2Ahead; ++t) prefetch(t);
       for (int t = 0; t < nt; ++t) {
         const int st = t & 1, u = t >> 1;
-        prefetch(t + kL2Ahead);
         const uint32_t empty = smem_u32(is_v ? &hdr->v_empty[st] : &hdr->k_empty[st]);
         if (u > 0 && !mbar_wait(empty, (u - 1) & 1)) {
           report(p.dev_status, DFLASH_ERR_TIMEOUT);
