@@ -62,3 +62,17 @@ def test_workspace_merge_equals_cluster_merge(dfl, wl):
     assert torch.equal(l_g, l_c)
     assert torch.equal(d_g, d_c)
     assert np.isfinite(l_g.cpu().numpy()).all()
+
+
+def test_workspace_merge_with_more_splits_than_lanes_matches_the_oracle(dfl):
+    """Two KV heads and a 12K context: one split per SM gives 47 splits per
+    (sequence, KV head), more than a warp has lanes, so the merge kernel's
+    (m, l) pairs span two registers per lane."""
+    from tests.test_gpu_configs import check_draft, f64_weights, fill_cache
+    wl = synth.Workload("small_bf16_L2_kv2_ctx12k", n_layers=2, d_target=128, n_taps=5, d_model=256,
+                        n_q_heads=8, n_kv_heads=2, head_dim=64, d_ffn=384, vocab=1003, gamma=16,
+                        dtype="bf16", batch=1, ctx=12000, seed=29)
+    gd = H.GpuDrafter(dfl, wl, max_rows=64)
+    lens = [wl.ctx]
+    k, v = fill_cache(gd, lens, "merge47")
+    check_draft(gd, f64_weights(gd.W), synth.anchors(wl), lens, k, v, [0])
