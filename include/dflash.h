@@ -130,9 +130,9 @@ typedef struct {
   double* flops;   /* host [capacity] algorithmic flops per launch     */
 } dflash_trace;
 
-/* Paged KV cache (SURVEY's NEXT row "paged / ragged KV-cache layout" for
- * serving-style continuous batching; the pages describe the cache only as
- * computed once per position and reused, [P1] "추론 구조"). Each layer's K
+/* Paged KV cache (a ragged layout for serving-style continuous batching,
+ * without padding every sequence to one capacity; the pages describe the
+ * cache only as computed once per position and reused, [P1] "추론 구조"). Each layer's K
  * and V live in a pool of pages of DFLASH_PAGE_KEYS positions:
  *   pool[L][n_pages][Hkv][DFLASH_PAGE_KEYS][Dh]  (cfg.dtype)
  * and position p of sequence b in page page_table[b * pages_per_seq + p /
@@ -259,9 +259,9 @@ dflash_status dflash_draft_block_paged(const dflash_config* cfg, const dflash_we
                                        void* ws, size_t ws_bytes, dflash_trace* trace,
                                        dflash_stream_t stream);
 
-/* Drafting pass with a block size per sequence (SURVEY's NEXT row "dynamic
- * gamma"; [P1] block-size ablation: a drafter trained with block 16 serves
- * smaller inference blocks, which makes per-request block sizes possible;
+/* Drafting pass with a block size per sequence ([P1] block-size ablation:
+ * a drafter trained with block 16 serves smaller inference blocks, which
+ * makes per-request block sizes possible;
  * the scheduling policy itself is left to the caller). Sequence b drafts
  * the block [anchor_b, m x gamma_b[b]] at positions ctx_len[b] + 0..gamma_b[b]:
  * exactly dflash_draft_block with gamma = gamma_b[b] for that sequence. Rows
