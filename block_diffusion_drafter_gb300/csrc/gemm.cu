@@ -282,7 +282,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
       const int nq = e.n_q_heads * Dh, nk = e.n_kv_heads * Dh;
       constexpr int kB = epi_batch<kOp, kWide>();
       for (int base = etid; base < total; base += 128 * kB) {
-        float y[kB], cs[kB], sn[kB];
+        float y[kB], cs[kB];  // value and its RoPE partner
         size_t o[kB];
         int kind[kB];  // 0 skip, 1 q, 2 k, 3 v
         int dd[kB], pp[kB], xx[kB];
@@ -358,7 +358,6 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           void* dst = kind[u] == 1 ? e.out : (kind[u] == 2 ? e.k_cache : e.v_cache);
           store_out(dst, e.out_bf16, o[u], val);
         }
-        (void)sn;
       }
       break;
     }
@@ -785,7 +784,6 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   // tile must pair each token's hi and lo columns inside one drain
   if (b_split && p.splits == 1 && p.bn > kBM)
     return plan_gemm(m_tiles, n_rows, k, elem_bytes, num_sms, allow_split, bn_cap, false);
-  p.partial_bytes = 0;
   return p;
 }
 

@@ -109,7 +109,6 @@ struct GemmPlan {
   int bn, n_sub, splits, kt_per_split, m_tiles, n_tiles, stages;
   int b_split;        // B tile packs hi and lo rows (bn covers 2 n_rows)
   size_t smem_bytes;
-  size_t partial_bytes;
 };
 
 // Chooses tile shape, split count and pipeline depth for m_tiles A tiles
