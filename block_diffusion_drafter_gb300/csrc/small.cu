@@ -194,7 +194,26 @@ __global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int3
   unsigned long long best = 0ull;
   constexpr int kVec = 16 / sizeof(T);
   if ((V % kVec) == 0 && (chunk % kVec) == 0) {
-    for (int v = v0 + threadIdx.x * kVec; v < v1; v += blockDim.x * kVec) {
+    // four 16-byte loads in flight per thread before any is compared: the
+    // scan is latency-bound, not bandwidth-bound, at a few loads per thread
+    constexpr int kIn = 4;
+    const int stride = blockDim.x * kVec;
+    int v = v0 + threadIdx.x * kVec;
+    for (; v + (kIn - 1) * stride < v1; v += kIn * stride) {
+      uint4 raw[kIn];
+#pragma unroll
+      for (int u = 0; u < kIn; ++u) raw[u] = __ldg(reinterpret_cast<const uint4*>(row + v + u * stride));
+#pragma unroll
+      for (int u = 0; u < kIn; ++u) {
+        const T* e = reinterpret_cast<const T*>(&raw[u]);
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          const unsigned long long k = argmax_key(to_f32(e[q]), static_cast<uint32_t>(v + u * stride + q));
+          best = k > best ? k : best;
+        }
+      }
+    }
+    for (; v < v1; v += stride) {
       const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + v));
       const T* e = reinterpret_cast<const T*>(&raw);
 #pragma unroll
