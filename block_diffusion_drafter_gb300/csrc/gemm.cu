@@ -820,6 +820,9 @@ cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, cons
   if (args.tf32 && split) return cudaErrorInvalidValue;  // split operands are bf16 only
   if (split != (plan.b_split != 0)) return cudaErrorInvalidValue;  // plan sized the other ring
   if (args.epi.op < 0 || args.epi.op >= kNumEpiOps) return cudaErrorInvalidValue;
+  // tokens along A rows: the fusion epilogue files its sums of squares per
+  // 128-feature group, so a B tile must hold whole groups
+  if (!args.swap && args.epi.op == EPI_FUSE && plan.bn % kBM != 0) return cudaErrorInvalidValue;
   const int variant = args.tf32 ? 0 : (split ? 2 : 1);
   const int wide = wide_tile(args) ? 1 : 0;
   const GemmKernel kern = kGemmKernels[wide][variant][args.epi.op];

@@ -225,6 +225,8 @@ dflash_status dflash_kv_inject(const dflash_config* cfg, const dflash_weights* w
  *     h += W_o o;  f = RMSNorm(h);  h += W_down(silu(W_gate f) * W_up f)
  *   z = RMSNorm(h[mask rows]); draft = argmax_V(W_lm z) (lowest index on ties)
  * anchor:  device [B] token ids; ctx_len: device [B] (not modified).
+ *   B * (gamma + 1) <= 512 (one projection tile spans all rows of a pass),
+ *   else DFLASH_ERR_TOO_LARGE; the same holds for every drafting call below.
  * max_ctx_hint: host upper bound of ctx_len[b] used to size the split-KV grid
  *   (any value is correct; a tight one is faster). Must be >= 0.
  * k_cache, v_cache: as in dflash_kv_inject. The block's own K/V rows are

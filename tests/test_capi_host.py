@@ -186,3 +186,19 @@ def test_paged_calls_reject_missing_or_short_page_views(lib):
                                           fake, fake, 1 << 30, None, None) == lib.ERR_INVALID_ARG
         assert L.dflash_kv_inject_paged(ctypes.byref(cfg), ctypes.byref(w), fake, fake, 1, 4, fake, arg, fake, fake,
                                         1 << 30, None, None) == lib.ERR_INVALID_ARG
+
+
+def test_drafting_passes_wider_than_one_tile_are_refused(lib):
+    """B * (gamma + 1) rows must fit one projection tile (512): 31 sequences of
+    17 rows are refused before anything else is looked at."""
+    wl = synth.WORKLOADS["qwen3_8b_L5_N2048_B1"].replace(batch=40)
+    cfg = lib.config_from_workload(wl)
+    w = lib.WeightsStruct()
+    L = lib.load()
+    assert lib.dflash_check_config(cfg) == lib.OK
+    for B, want in [(31, lib.ERR_TOO_LARGE), (40, lib.ERR_TOO_LARGE)]:
+        assert L.dflash_draft_block(ctypes.byref(cfg), ctypes.byref(w), None, None, B, 0, None, None,
+                                    None, None, None, None, None, 0, None, None) == want
+    # 30 sequences of 17 rows fit: the call proceeds to the argument checks
+    assert L.dflash_draft_block(ctypes.byref(cfg), ctypes.byref(w), None, None, 30, 0, None, None,
+                                None, None, None, None, None, 0, None, None) == lib.ERR_INVALID_ARG
