@@ -41,7 +41,8 @@ WsLayout ws_layout(const dflash_config* c) {
   L.act = take(parts * rows * static_cast<size_t>(c->d_ffn) * es);
   L.z = take(parts * static_cast<size_t>(c->max_batch) * c->gamma * D * es);
   L.ss = take(rows * (D / kBM) * 4);
-  L.lm_keys = take(static_cast<size_t>(c->max_batch) * c->gamma * 8);
+  // per (LM-head tile, mask row): the tile's packed argmax key
+  L.lm_keys = take(static_cast<size_t>((c->vocab + kBM - 1) / kBM) * c->max_batch * c->gamma * 8);
   L.v_keys = take(rows * 8);
   L.v_count = take(static_cast<size_t>(c->max_batch) * 4);
   L.samp = take(dfl::sample_ws_bytes(c->max_batch, c->gamma, c->vocab));
@@ -619,7 +620,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
 
   cx.tr.before(DFLASH_K_NORM, row_bytes + static_cast<double>(rows) * D * es, 0);
   st = fail(launch_embed(w->embed, anchor, ids, c->mask_token_id, B, R, D, V, bf16, h, gain_of(w->g_attn, 0),
-                         xn, xn_lo, ss, keys, nmask, dev_status, cx.s, cx.pdl));
+                         xn, xn_lo, ss, dev_status, cx.s, cx.pdl));
   cx.tr.after();
   if (st != DFLASH_OK) return st;
   if (layer_dump_opt != nullptr &&
@@ -748,6 +749,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
     g.epi = base_epi(c);
     g.epi.op = EPI_ARGMAX; g.epi.out = logits_opt; g.epi.ld = V; g.epi.n_tok = nmask; g.epi.n_feat = V;
     g.epi.keys = keys;
+    g.epi.keys_ld = (V + kBM - 1) / kBM;
     g.epi.gamma = c->gamma;
     g.epi.temperature = temperature;
     g.epi.seed = seed;
@@ -757,7 +759,8 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
       return st;
   }
   cx.tr.before(DFLASH_K_ARGMAX, nmask * 12.0, 0);
-  st = fail(launch_argmax_finalize(keys, nmask, c->gamma, gamma_b, draft, cx.s, cx.pdl));
+  st = fail(launch_argmax_finalize(keys, (V + kBM - 1) / kBM, (V + kBM - 1) / kBM, nmask, c->gamma, gamma_b, draft,
+                                   cx.s, cx.pdl));
   cx.tr.after();
   return st;
 }

@@ -390,7 +390,9 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
           best = o > best ? o : best;
         }
-        if (lane == 0 && tok < e.n_tok && best != 0ull) atomicMax(&e.keys[tok], best);
+        // one slot per (tile, token): no other CTA writes it, so no atomics
+        // (a shared slot per token took 1187 same-address atomics each)
+        if (lane == 0 && tok < e.n_tok) e.keys[static_cast<size_t>(tok) * e.keys_ld + m_tile] = best;
       }
       break;
     }

@@ -51,8 +51,10 @@ struct Epi {
   const float* rope_cos;
   const float* rope_sin;
   int rope_positions;
-  // EPI_ARGMAX
+  // EPI_ARGMAX: keys[tok * keys_ld + m_tile] = packed (value, index) max of
+  // token tok over the tile's 128 vocabulary entries (every entry written)
   unsigned long long* keys;
+  int keys_ld;
   // EPI_ARGMAX sampling mode (temperature > 0): token t = b * gamma + j ranks
   // vocabulary entry v by logit / temperature + Gumbel(seed, stream 0, j, b, v)
   float temperature;
@@ -166,12 +168,11 @@ cudaError_t launch_attention_merge(const AttnArgs& a, cudaStream_t stream, bool 
 // h[b*R + i] = embed[id] (id = ids[b*R + i] when ids is given, else anchor[b]
 // for i == 0 and mask_id otherwise), fp32; also xg = gain (.) h in cfg dtype
 // and ss[row][c] = sum of h^2 over features 128c..128c+127 (the first
-// layer's folded RMSNorm); zeroes keys[0..n_keys).
+// layer's folded RMSNorm).
 cudaError_t launch_embed(const void* embed, const int* anchor, const int* ids, int mask_id, int B, int R,
                          int D, int V,
                          int bf16, float* h, const void* gain, void* xg, size_t xg_lo_off, float* ss,
-                         unsigned long long* keys, int n_keys, int* dev_status, cudaStream_t s,
-                         bool pdl);
+                         int* dev_status, cudaStream_t s, bool pdl);
 // h[t] = gain * u[t] / sqrt(sum(row_ss[t]) / D + eps), u fp32, h in cfg dtype.
 cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
                              int T, int D, float eps, int bf16, cudaStream_t s, bool pdl);
@@ -203,10 +204,10 @@ cudaError_t launch_sample_verify(const void* target, int target_bf16, const floa
                                  const int32_t* draft, int B, int gamma, int V, float temperature,
                                  uint64_t seed, void* ws, int32_t* tau, int32_t* committed,
                                  int32_t* next_anchor, cudaStream_t s, bool pdl);
-// draft[t] = index of keys[t]; with gamma_b, t = b * gamma + j with j >= gamma_b[b] gets -1.
-cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int gamma, const int32_t* gamma_b,
-                                   int32_t* draft,
-                                   cudaStream_t s, bool pdl);
+// draft[t] = index of the max of keys[t * ld + 0 .. n_tiles) (the LM head's
+// per-tile maxima); with gamma_b, t = b * gamma + j with j >= gamma_b[b] gets -1.
+cudaError_t launch_argmax_finalize(const unsigned long long* keys, int n_tiles, int ld, int n, int gamma,
+                                   const int32_t* gamma_b, int32_t* draft, cudaStream_t s, bool pdl);
 cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
                               int reserve, int* dev_status, cudaStream_t s, bool pdl);
 // Greedy verify-accept; gamma_b NULL or [B] (sequence b verifies its first gamma_b[b] drafts).

@@ -67,7 +67,6 @@ template <typename T>
 __global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* anchor, const int* ids,
                                                     int mask_id, int R, int D, int V, float* h, const T* gain,
                                                     T* xg, size_t xg_lo_off, float* ss,
-                                                    unsigned long long* keys, int n_keys,
                                                     int* dev_status) {
   pdl_launch_dependents();
   pdl_wait();
@@ -105,8 +104,6 @@ __global__ void __launch_bounds__(256) embed_kernel(const T* embed, const int* a
     for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
     if ((threadIdx.x & 31) == 0 && q < n4) ss[static_cast<size_t>(r) * (D / 128) + q / 32] = sq;
   }
-  if (blockIdx.x == 0)
-    for (int k = threadIdx.x; k < n_keys; k += blockDim.x) keys[k] = 0ull;
 }
 
 template <typename T>
@@ -143,14 +140,43 @@ __device__ __forceinline__ int block_gamma(const int32_t* gamma_b, int b, int ga
   return gamma_b == nullptr ? gamma : min(max(gamma_b[b], 1), gamma);
 }
 
-__global__ void argmax_finalize_kernel(unsigned long long* keys, int n, int gamma, const int32_t* gamma_b,
-                                       int32_t* draft) {
+// Token i's argmax over the vocabulary: the max of the LM head's per-tile
+// keys[i * ld + t] (t < n_tiles, contiguous per token), one CTA per token,
+// every thread with all of its (up to kFinPer) loads in flight; the max of
+// packed keys is order-free.
+constexpr int kFinThreads = 128, kFinPer = 10;
+__global__ void __launch_bounds__(kFinThreads) argmax_finalize_kernel(const unsigned long long* keys, int n_tiles,
+                                                                      int ld, int n, int gamma,
+                                                                      const int32_t* gamma_b, int32_t* draft) {
+  __shared__ unsigned long long red[kFinThreads / 32];
   pdl_launch_dependents();
   pdl_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  draft[i] = i % gamma < block_gamma(gamma_b, i / gamma, gamma) ? static_cast<int32_t>(argmax_key_index(keys[i]))
-                                                                 : -1;
+  const int i = blockIdx.x;
+  const unsigned long long* row = keys + static_cast<size_t>(i) * ld;
+  unsigned long long best = 0ull;
+  for (int t0 = 0; t0 < n_tiles; t0 += kFinThreads * kFinPer) {
+    unsigned long long k[kFinPer];
+#pragma unroll
+    for (int u = 0; u < kFinPer; ++u) {
+      const int t = t0 + u * kFinThreads + static_cast<int>(threadIdx.x);
+      k[u] = t < n_tiles ? row[t] : 0ull;
+    }
+#pragma unroll
+    for (int u = 0; u < kFinPer; ++u) best = k[u] > best ? k[u] : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
+    best = x > best ? x : best;
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 1; w < kFinThreads / 32; ++w) best = red[w] > best ? red[w] : best;
+    draft[i] = i % gamma < block_gamma(gamma_b, i / gamma, gamma) ? static_cast<int32_t>(argmax_key_index(best))
+                                                                   : -1;
+  }
 }
 
 __global__ void kv_advance_kernel(int32_t* ctx_len, const int32_t* n_new, int B, int Tmax, int ncap,
@@ -273,17 +299,16 @@ __global__ void __launch_bounds__(256) verify_kernel(const T* logits, const int3
 cudaError_t launch_embed(const void* embed, const int* anchor, const int* ids, int mask_id, int B, int R,
                          int D, int V,
                          int bf16, float* h, const void* gain, void* xg, size_t xg_lo_off, float* ss,
-                         unsigned long long* keys, int n_keys, int* dev_status, cudaStream_t s,
-                         bool pdl) {
+                         int* dev_status, cudaStream_t s, bool pdl) {
   if (bf16)
     return launch_ex(embed_kernel<__nv_bfloat16>, dim3(B * R), dim3(256), 0, s, pdl,
                      reinterpret_cast<const __nv_bfloat16*>(embed), anchor, ids, mask_id, R, D, V, h,
                      reinterpret_cast<const __nv_bfloat16*>(gain), reinterpret_cast<__nv_bfloat16*>(xg),
-                     xg_lo_off, ss, keys, n_keys, dev_status);
+                     xg_lo_off, ss, dev_status);
   return launch_ex(embed_kernel<float>, dim3(B * R), dim3(256), 0, s, pdl,
                    reinterpret_cast<const float*>(embed), anchor, ids, mask_id, R, D, V, h,
                    reinterpret_cast<const float*>(gain), reinterpret_cast<float*>(xg), size_t(0), ss,
-                   keys, n_keys, dev_status);
+                   dev_status);
 }
 
 cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n_ss, const void* gain,
@@ -296,9 +321,9 @@ cudaError_t launch_fuse_norm(const float* u, void* h, const float* row_ss, int n
                    row_ss, n_ss, reinterpret_cast<const float*>(gain), D, eps);
 }
 
-cudaError_t launch_argmax_finalize(unsigned long long* keys, int n, int gamma, const int32_t* gamma_b,
-                                   int32_t* draft, cudaStream_t s, bool pdl) {
-  return launch_ex(argmax_finalize_kernel, dim3((n + 127) / 128), dim3(128), 0, s, pdl, keys, n, gamma,
+cudaError_t launch_argmax_finalize(const unsigned long long* keys, int n_tiles, int ld, int n, int gamma,
+                                   const int32_t* gamma_b, int32_t* draft, cudaStream_t s, bool pdl) {
+  return launch_ex(argmax_finalize_kernel, dim3(n), dim3(kFinThreads), 0, s, pdl, keys, n_tiles, ld, n, gamma,
                    gamma_b, draft);
 }
 
