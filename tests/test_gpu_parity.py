@@ -147,6 +147,12 @@ def test_chain_small_bf16_rope_off(dfl):
     run_chain(dfl, SMALL.replace(rope_theta=0.0, batch=1), [130])
 
 
+def test_chain_small_bf16_vocab_over_1280_tiles(dfl):
+    # 200003 entries = 1563 LM-head tiles (the last one 67 rows): the per-token
+    # reduction of the tiles' argmax keys takes more than one pass of its CTA
+    run_chain(dfl, SMALL.replace(n_layers=1, batch=2, vocab=200003), [64, 9], check_dumps=False)
+
+
 MEDIUM = synth.Workload("medium_bf16_L2", n_layers=2, d_target=512, n_taps=5, d_model=1024,
                         n_q_heads=8, n_kv_heads=2, head_dim=128, d_ffn=2048, vocab=5000, gamma=16,
                         dtype="bf16", batch=2, ctx=1000, seed=9)
