@@ -2,11 +2,9 @@
 that include/dflash.h declares, and its pure-host calls (config checks,
 sizing, RoPE tables, argument validation) behave without a GPU."""
 import ctypes
-import math
 import os
 
 import numpy as np
-import pytest
 
 import synth
 
