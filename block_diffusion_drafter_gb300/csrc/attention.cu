@@ -91,15 +91,16 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs p) {
 
 }  // namespace
 
-void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
-                    int* chunk, int* merge_global) {
+void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int num_sms,
+                    int* splits, int* chunk, int* merge_global) {
   const int n_keys = (max_ctx < ncap ? max_ctx : ncap) + R;
   const int per_seq = B * Hkv > 0 ? B * Hkv : 1;
   const int tiles = (n_keys + 127) / 128;
   // Long contexts with few (sequence, KV head) pairs: a cluster of at most
   // kMaxAttnCluster splits per pair would leave SMs idle, so take one split
   // per SM (each at least two 128-key tiles) and merge through the workspace.
-  int wide = 152 / per_seq;
+  const int sms = num_sms > 0 ? num_sms : 1;
+  int wide = sms / per_seq;
   if (wide > kAttnMaxSlots / per_seq) wide = kAttnMaxSlots / per_seq;
   if (wide > tiles / 2) wide = tiles / 2;
   int sp, c;
@@ -112,7 +113,7 @@ void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap
   } else if (global) {
     sp = wide;
   } else {
-    sp = (2 * 152 + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
+    sp = (2 * sms + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
     if (sp > kMaxAttnCluster) sp = kMaxAttnCluster;
   }
   // whole 128-key tiles per split (the tcgen05 kernel's tile)

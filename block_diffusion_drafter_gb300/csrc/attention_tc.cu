@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  int issued = 0;  // producer lanes: tiles whose TMA loads were issued
   const int G = p.n_q_heads / p.n_kv_heads;
   const int n_q = G * p.R;
 
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_expect_tx(bar, kTileBytes);
 #pragma unroll
         for (int j = 0; j < NSUB; ++j) tma_load_3d(dst + j * kSub, map, bar, 64 * j, y, z, pol);
+        issued = t + 1;
       }
     }
     __syncwarp();
@@ -503,6 +505,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     cluster_arrive();
   }
   __syncthreads();
+  // after a timeout, no TMA load of this CTA may still be landing when it
+  // exits: each producer lane waits (bounded) for the last two tiles of its
+  // ring; earlier tiles of a stage completed before the stage was refilled
+  if (warp == 0 && lane < 2 && *abort_flag) {
+    for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
+      mbar_wait(smem_u32(lane == 1 ? &hdr->v_full[t & 1] : &hdr->k_full[t & 1]), (t >> 1) & 1);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

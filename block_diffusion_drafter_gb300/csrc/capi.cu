@@ -516,8 +516,6 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
   dflash_status st = dflash_check_config(c);
   if (st != DFLASH_OK) return st;
   if (w == nullptr || B < 1 || B > c->max_batch || max_ctx_hint < 0) return DFLASH_ERR_INVALID_ARG;
-  // one projection tile spans all B * (gamma + 1) rows of a pass
-  if (B * (c->gamma + 1) > kMaxBN) return DFLASH_ERR_TOO_LARGE;
   if ((anchor == nullptr && ids == nullptr) || ctx_len == nullptr || k_cache == nullptr || v_cache == nullptr ||
       draft == nullptr || dev_status == nullptr || w->embed == nullptr || w->g_final == nullptr ||
       w->lm_head == nullptr || w->g_attn == nullptr || w->w_qkv == nullptr || w->w_o == nullptr ||
@@ -628,7 +626,7 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
     return DFLASH_ERR_CUDA;
 
   int a_splits = 1, a_chunk = 0, a_global = 0;
-  plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, ncap,
+  plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, ncap, cx.sms,
                  &a_splits, &a_chunk, &a_global);
 
   for (int l = 0; l < Lyr; ++l) {

@@ -330,7 +330,14 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
               if (kind[u] != 3 && e.rope_cos != nullptr) {
                 const int pa = g.swap ? (d < half ? a + half : a - half) : a;
                 const int pb = g.swap ? b : (d < half ? b + half : b - half);
-                cs[u] = S[pb * kSLD + pa];   // partner value, rotated below
+                if (pa < 0 || pa >= kBM || pb < 0 || pb >= cols) {
+                  // the RoPE partner lies outside the staged chunk: a head
+                  // split across chunks, which the launcher refuses
+                  report(g.dev_status, DFLASH_ERR_SHAPE);
+                  kind[u] = 0;
+                } else {
+                  cs[u] = S[pb * kSLD + pa];   // partner value, rotated below
+                }
               }
             }
           }
@@ -434,6 +441,7 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
   constexpr int kBK = kTF32 ? 32 : 64;  // 128 bytes of k per row either way
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x, split = blockIdx.y, n_tile = blockIdx.z;
+  int issued = 0;  // producer: k-steps whose TMA loads were issued
   const int KT = g.k / kBK;
   const int kt0 = split * g.kt_per_split;
   const int nkt = min(g.kt_per_split, KT - kt0);
@@ -515,6 +523,7 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
       }
       pdl_wait();
       for (int it = 0; it < n_pre; ++it) load_b(it, kt0 + it);
+      issued = n_pre;
       for (int it = n_pre; it < nkt; ++it) {
         const int s = it % stages, u = it / stages;
         if (u > 0 && !mbar_wait(smem_u32(&hdr->empty[s]), (u - 1) & 1)) {
@@ -526,6 +535,7 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
         mbar_expect_tx(smem_u32(&hdr->full[s]), stage_tx);
         load_a(s, kt0 + it);
         load_b(s, kt0 + it);
+        issued = it + 1;
       }
     }
     __syncwarp();
@@ -679,6 +689,14 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
     cluster_wait();
   }
   __syncthreads();
+  // A CTA that gave up a bounded wait must not exit while TMA loads it issued
+  // can still land in its shared memory: the producer waits (bounded again)
+  // for the transactions of the last `stages` k-steps it issued. Earlier
+  // k-steps of the same stages completed before their stage was refilled.
+  if (warp == 0 && lane == 0 && *reinterpret_cast<volatile int*>(&hdr->abort_flag)) {
+    for (int it = issued > stages ? issued - stages : 0; it < issued; ++it)
+      mbar_wait(smem_u32(&hdr->full[it % stages]), (it / stages) & 1);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
@@ -822,9 +840,17 @@ cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, cons
   if (args.tf32 && split) return cudaErrorInvalidValue;  // split operands are bf16 only
   if (split != (plan.b_split != 0)) return cudaErrorInvalidValue;  // plan sized the other ring
   if (args.epi.op < 0 || args.epi.op >= kNumEpiOps) return cudaErrorInvalidValue;
-  // tokens along A rows: the fusion epilogue files its sums of squares per
-  // 128-feature group, so a B tile must hold whole groups
-  if (!args.swap && args.epi.op == EPI_FUSE && plan.bn % kBM != 0) return cudaErrorInvalidValue;
+  // Tokens along A rows (features along B rows): the epilogue stages 128
+  // accumulator columns at a time, so a B tile must hold whole 128-feature
+  // groups -- the fusion files its sums of squares per group, and RoPE pairs
+  // feature d of a head with d +- Dh/2 inside the staged chunk. Injection
+  // tiles must also not straddle two layers' features.
+  if (!args.swap && (args.epi.op == EPI_FUSE || args.epi.op == EPI_QKV || args.epi.op == EPI_KV) &&
+      plan.bn % kBM != 0)
+    return cudaErrorInvalidValue;
+  if (!args.swap && args.epi.op == EPI_KV &&
+      (args.epi.feat_per_layer % plan.bn != 0 || args.b_tiles_per_z * plan.bn != args.epi.feat_per_layer))
+    return cudaErrorInvalidValue;
   const int variant = args.tf32 ? 0 : (split ? 2 : 1);
   const int wide = wide_tile(args) ? 1 : 0;
   const GemmKernel kern = kGemmKernels[wide][variant][args.epi.op];

@@ -156,8 +156,10 @@ __host__ __device__ constexpr size_t attn_slot_floats(int head_dim) {
 }
 // Partial-result slots in a workspace: B * Hkv * splits on the merge_global path.
 constexpr int kAttnMaxSlots = 160;
-void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int* splits,
-                    int* chunk, int* merge_global);
+// Split-KV plan for B sequences over at most max_ctx context keys on a device
+// with num_sms SMs.
+void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap, int num_sms,
+                    int* splits, int* chunk, int* merge_global);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream, bool pdl);
 // bf16 path on tcgen05 (attention_tc.cu)
 cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl);
@@ -222,6 +224,7 @@ int num_sms_of_current_device();
 dflash_status check_arch();
 // Programmatic dependent launch on (default) unless DFLASH_PDL=0.
 bool use_pdl();
-int verify_chunks(int B, int R, int V);
+// V-chunks per target row of verify_kernel: about two CTAs per SM in total.
+int verify_chunks(int B, int R, int V, int num_sms);
 
 }  // namespace dfl

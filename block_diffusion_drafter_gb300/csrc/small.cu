@@ -337,9 +337,9 @@ cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t
   return launch_ex(copy_f32_kernel, dim3(304), dim3(256), 0, s, pdl, dst, src, n);
 }
 
-int verify_chunks(int B, int R, int V) {
+int verify_chunks(int B, int R, int V, int num_sms) {
   int by_size = (V + 4095) / 4096;
-  int by_grid = (2 * 152 + B * R - 1) / (B * R);
+  int by_grid = (2 * (num_sms > 0 ? num_sms : 1) + B * R - 1) / (B * R);
   int c = by_size < by_grid ? by_size : by_grid;
   return c < 1 ? 1 : c;
 }
@@ -349,7 +349,7 @@ cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, co
                           int32_t* next_anchor, unsigned long long* keys, int* counters,
                           cudaStream_t s, bool pdl) {
   const int R = gamma + 1;
-  const int chunks = verify_chunks(B, R, V);
+  const int chunks = verify_chunks(B, R, V, num_sms_of_current_device());
   int chunk = (V + chunks - 1) / chunks;
   chunk = (chunk + 7) / 8 * 8;
   const int n_chunks = (V + chunk - 1) / chunk;
@@ -363,9 +363,18 @@ cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, co
 }
 
 int num_sms_of_current_device() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  // SM count of each device, queried once (0: not yet known). A failed query
+  // gives 1: plans stay valid, only the grid sizing is poorer, and the launch
+  // that follows reports the device error itself.
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  int& n = cached[dev & 63];
+  if (n == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 1;
+    n = v;
+  }
   return n;
 }
 

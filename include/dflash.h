@@ -224,9 +224,9 @@ dflash_status dflash_kv_inject(const dflash_config* cfg, const dflash_weights* w
  *         inside the block, every row sees all ctx_len[b] + R keys);
  *     h += W_o o;  f = RMSNorm(h);  h += W_down(silu(W_gate f) * W_up f)
  *   z = RMSNorm(h[mask rows]); draft = argmax_V(W_lm z) (lowest index on ties)
- * anchor:  device [B] token ids; ctx_len: device [B] (not modified).
- *   B * (gamma + 1) <= 512 (one projection tile spans all rows of a pass),
- *   else DFLASH_ERR_TOO_LARGE; the same holds for every drafting call below.
+ * anchor:  device [B] token ids, 1 <= B <= cfg.max_batch; ctx_len: device [B]
+ *   (not modified). A pass of up to 512 block rows (B * (gamma + 1)) runs as
+ *   one projection tile of tokens; larger passes take several 256-row tiles.
  * max_ctx_hint: host upper bound of ctx_len[b] used to size the split-KV grid
  *   (any value is correct; a tight one is faster). Must be >= 0.
  * k_cache, v_cache: as in dflash_kv_inject. The block's own K/V rows are
@@ -413,10 +413,12 @@ dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, fl
  * Scratch: a fixed array in the library's device memory (about 140 KB per GPU
  * that loads the library, held until the process exits) instead of `ws`.
  * Limits: B <= 1024 and B * (gamma + 1) <= 16384, else DFLASH_ERR_TOO_LARGE
- * and nothing is launched.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. Each call clears the part of the array it uses
+ * and nothing is launched; B <= cfg.max_batch as for dflash_verify_accept
+ * (else DFLASH_ERR_INVALID_ARG).
+ * Every call looks up the array's address in the current context
+ * (cudaGetSymbolAddress, a host-side lookup); the first call in a context
+ * loads the library's device code there, so make it before any stream
+ * capture. Each call clears the part of the array it uses
  * (cudaMemsetAsync on `stream`) and allocates nothing. All calls share the
  * one array, which keeps the last call's contents: calls whose work overlaps
  * on the GPU (different streams, or concurrent graphs) race on it and must be

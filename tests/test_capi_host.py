@@ -186,17 +186,24 @@ def test_paged_calls_reject_missing_or_short_page_views(lib):
                                         1 << 30, None, None) == lib.ERR_INVALID_ARG
 
 
-def test_drafting_passes_wider_than_one_tile_are_refused(lib):
-    """B * (gamma + 1) rows must fit one projection tile (512): 31 sequences of
-    17 rows are refused before anything else is looked at."""
+def test_drafting_batch_limit_is_the_configured_max_batch(lib):
+    """A drafting pass takes any B up to cfg.max_batch, including passes of more
+    than 512 block rows (several token tiles); B above max_batch (or below 1)
+    is refused before anything else is looked at. With null pointers an
+    accepted B proceeds to the pointer checks (ERR_INVALID_ARG as well, so the
+    accepted sizes are told apart by a config whose max_batch is smaller)."""
     wl = synth.WORKLOADS["qwen3_8b_L5_N2048_B1"].replace(batch=40)
-    cfg = lib.config_from_workload(wl)
     w = lib.WeightsStruct()
     L = lib.load()
-    assert lib.dflash_check_config(cfg) == lib.OK
-    for B, want in [(31, lib.ERR_TOO_LARGE), (40, lib.ERR_TOO_LARGE)]:
+    small = lib.config_from_workload(wl.replace(batch=30))
+    big = lib.config_from_workload(wl)
+    assert lib.dflash_check_config(big) == lib.OK
+    for cfg, B in [(small, 31), (small, 0), (big, 41)]:
         assert L.dflash_draft_block(ctypes.byref(cfg), ctypes.byref(w), None, None, B, 0, None, None,
-                                    None, None, None, None, None, 0, None, None) == want
-    # 30 sequences of 17 rows fit: the call proceeds to the argument checks
-    assert L.dflash_draft_block(ctypes.byref(cfg), ctypes.byref(w), None, None, 30, 0, None, None,
-                                None, None, None, None, None, 0, None, None) == lib.ERR_INVALID_ARG
+                                    None, None, None, None, None, 0, None, None) == lib.ERR_INVALID_ARG
+    # 40 sequences of 17 rows (680 > 512) pass the size checks and stop at the
+    # first null pointer, which is not a size error
+    for B in (30, 31, 40):
+        st = L.dflash_draft_block(ctypes.byref(big), ctypes.byref(w), None, None, B, 0, None, None,
+                                  None, None, None, None, None, 0, None, None)
+        assert st == lib.ERR_INVALID_ARG and st != lib.ERR_TOO_LARGE

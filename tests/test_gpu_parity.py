@@ -175,3 +175,19 @@ def test_chain_tiny_f32(dfl):
 def test_chain_qwen3_8b_N2048(dfl):
     wl = synth.WORKLOADS["qwen3_8b_L5_N2048_B1"]
     run_chain(dfl, wl, [wl.ctx], check_dumps=True)
+
+
+def test_chain_small_bf16_batch_32_several_token_tiles(dfl):
+    # 32 sequences x 17 rows = 544 block rows: every drafting projection takes
+    # three 256-row token tiles (the last one 32 rows), the LM head one
+    # 512-row tile; ragged contexts, some empty
+    lens = [int(x) for x in np.random.default_rng(32).integers(0, 160, size=32)]
+    lens[3] = 0
+    run_chain(dfl, SMALL.replace(n_layers=1, batch=32, ctx=160), lens, check_dumps=True)
+
+
+def test_chain_medium_bf16_batch_40_lm_head_several_tiles(dfl):
+    # 40 x 17 = 680 block rows and 640 mask rows: the LM head's token rows
+    # span three tiles too; K = 1024..2048 splits the projections over clusters
+    lens = [int(x) for x in np.random.default_rng(40).integers(1, 90, size=40)]
+    run_chain(dfl, MEDIUM.replace(n_layers=1, batch=40, ctx=90), lens, check_dumps=False)
