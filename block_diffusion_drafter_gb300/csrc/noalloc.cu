@@ -25,9 +25,6 @@ struct VerifyScratch {
 // device address: only the address from cudaGetSymbolAddress is passed on.
 static __device__ __align__(256) VerifyScratch g_verify_scratch;
 
-VerifyScratch* g_scratch_addr[64];
-bool g_scratch_ready[64];
-
 }  // namespace
 
 extern "C" dflash_status dflash_verify_accept_noalloc(const dflash_config* c,
@@ -45,18 +42,17 @@ extern "C" dflash_status dflash_verify_accept_noalloc(const dflash_config* c,
   const int R = c->gamma + 1;
   if (B > kNoAllocMaxSeqs || static_cast<long long>(B) * R > kNoAllocMaxRows)
     return DFLASH_ERR_TOO_LARGE;
+  if (B > c->max_batch) return DFLASH_ERR_INVALID_ARG;  // as dflash_verify_accept
   if ((st = dfl::check_arch()) != DFLASH_OK) return st;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFLASH_ERR_CUDA;
-  if (!g_scratch_ready[dev]) {
-    // once per device, with that device current
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr)
-      return DFLASH_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<VerifyScratch*>(p);
-    g_scratch_ready[dev] = true;
-  }
-  VerifyScratch* s = g_scratch_addr[dev];
+  // The array's address in the current context, looked up on every call (a
+  // host-side lookup once the module is loaded): an address kept from an
+  // earlier call could belong to another context of the same device, or to
+  // a context that cudaDeviceReset has since destroyed. The first call in a
+  // context loads the module; make it before any stream capture.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr)
+    return DFLASH_ERR_CUDA;
+  VerifyScratch* s = static_cast<VerifyScratch*>(p);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   // the keys and counters of this call must start at zero
   if (cudaMemsetAsync(s->keys, 0, sizeof(unsigned long long) * B * R, cs) != cudaSuccess ||

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import synth
+from oracle import dflash_ref as ref
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +57,47 @@ def test_noalloc_verify_matches_workspace_verify(lib, dtype):
         for a, b in zip(outs[0], outs[1]):
             np.testing.assert_array_equal(a, b)   # integer outputs: exact
         assert (outs[1][0] >= 1).all() and (outs[1][0] <= R).all()
+        # and both are the oracle's greedy acceptance
+        d_np = draft.cpu().numpy()
+        for b in range(B):
+            t, c, n = ref.verify_accept(logits[b].float().cpu(), d_np[b])
+            assert int(outs[1][0][b]) == t and int(outs[1][2][b]) == n
+            np.testing.assert_array_equal(outs[1][1][b], c)
+
+
+def _both(lib, cfg, ws, logits, draft):
+    """(tau, committed, next anchor) of the workspace call and of the
+    allocation-free call on the same inputs."""
+    B, R = logits.shape[0], logits.shape[1]
+    outs = []
+    for fn in ("ws", "noalloc"):
+        tau = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        committed = torch.full((B, R), -7, dtype=torch.int32, device="cuda")
+        nxt = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+        if fn == "ws":
+            lib.dflash_verify_accept(cfg, logits, draft, tau, committed, nxt, ws)
+        else:
+            lib.dflash_verify_accept_noalloc(cfg, logits, draft, tau, committed, nxt)
+        torch.cuda.synchronize()
+        outs.append((tau.cpu().numpy(), committed.cpu().numpy(), nxt.cpu().numpy()))
+    return outs
+
+
+def test_noalloc_verify_at_the_array_edge_and_after_larger_calls(lib):
+    """963 sequences of 17 rows (16371 of the array's 16384 key slots), then a
+    small call, then the full-size call again: every call must match the
+    workspace call, whatever an earlier, larger call left in the array."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    wl = WL.replace(vocab=1003, batch=963)
+    cfg = lib.config_from_workload(wl)
+    ws = lib.Workspace(cfg, 16)
+    for call, B in enumerate([963, 5, 963, 1]):
+        logits, draft = planted(wl.replace(batch=B), 200 + call, torch.float32)
+        outs = _both(lib, cfg, ws, logits, draft)
+        for a, b in zip(outs[0], outs[1]):
+            np.testing.assert_array_equal(a, b)
+        assert (outs[1][0] >= 1).all() and (outs[1][0] <= wl.rows).all()
 
 
 def test_noalloc_verify_rejects_oversized_batches(lib):
