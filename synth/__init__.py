@@ -216,21 +216,39 @@ def splitmix64(x: int) -> int:
     return z ^ (z >> 31)
 
 
-def loop_plan(wl: Workload, cycle: int, p_agree: float = 0.8):
-    """Per (b, j): whether the synthetic target agrees with draft token j
-    (Bernoulli(p_agree); never for the bonus row j = gamma) and an offset
-    in [1, V-1] that picks a different token when it does not.
-    Returns (agree [B, R] bool, offset [B, R] int64)."""
+P_AGREE_16 = 52429   # agreement threshold on a 16-bit hash: 52429 / 65536 = 0.8
+
+
+def loop_plan(wl: Workload, cycle: int):
+    """Per (b, j) of one loop cycle: a 16-bit key and an offset in [1, V-1].
+    The synthetic target agrees with draft token j when
+    (draft_j * 40503 + key) mod 2^16 < P_AGREE_16 (probability 0.8 over the
+    key for every token value, never for the bonus row j = gamma), so whether
+    it agrees depends on the drafted token itself; where it does not agree it
+    picks (draft_j + offset) mod V, a different token.
+    Returns (key16 [B, R] int64, offset [B, R] int64)."""
     B, R, V = wl.batch, wl.rows, wl.vocab
-    agree = np.zeros((B, R), dtype=bool)
+    key16 = np.zeros((B, R), dtype=np.int64)
     offset = np.zeros((B, R), dtype=np.int64)
     for b in range(B):
         for j in range(R):
             key = splitmix64(((wl.seed * 1000003 + cycle) * 4099 + b) * 131 + j)
-            u = (key >> 11) / float(1 << 53)
-            agree[b, j] = (j < R - 1) and (u < p_agree)
+            key16[b, j] = key >> 48
             offset[b, j] = 1 + (splitmix64(key) % (V - 1))
-    return agree, offset
+    return key16, offset
+
+
+def loop_intended(wl: Workload, key16: torch.Tensor, offset: torch.Tensor,
+                  draft: torch.Tensor) -> torch.Tensor:
+    """[n, R] int64 tokens the synthetic target makes its argmax, for drafts
+    [n, gamma] (any device; integer arithmetic only, so every device gives
+    the same tokens). key16 / offset: [n, R] int64 from loop_plan."""
+    n, R = draft.shape[0], wl.rows
+    base = torch.zeros((n, R), dtype=torch.int64, device=draft.device)
+    base[:, : R - 1] = draft.to(torch.int64)
+    agree = ((base * 40503 + key16) & 0xFFFF) < P_AGREE_16
+    agree[:, R - 1] = False
+    return torch.where(agree, base, (base + offset) % wl.vocab)
 
 
 def loop_target_logits(wl: Workload, cycle: int, draft: torch.Tensor, seqs=None,
@@ -238,21 +256,16 @@ def loop_target_logits(wl: Workload, cycle: int, draft: torch.Tensor, seqs=None,
     """[len(seqs), R, V] synthetic target logits for one loop cycle (all B
     sequences when seqs is None; draft holds the drafts of those sequences).
 
-    N(0,1) noise, then the "intended" token of row j gets max(row) + 1 so it
-    is the unique argmax: draft[b, j] where loop_plan says agree, otherwise
-    (draft[b, j] + offset) mod V, which differs from the draft token. Uses
-    only integer indexing and one max per row, on draft's device."""
+    N(0,1) noise, then the token loop_intended picks for row j gets
+    max(row) + 1, so it is the unique argmax. Uses only integer arithmetic,
+    indexing and one max per row, on draft's device."""
     dev = draft.device
-    B, R, V = wl.batch, wl.rows, wl.vocab
+    B = wl.batch
     seqs = list(range(B)) if seqs is None else list(seqs)
-    noise = normal((B, R, V), wl.seed, f"loop_noise/{cycle}", dev)[seqs]
-    agree, offset = loop_plan(wl, cycle)
-    agree_t = torch.as_tensor(agree[seqs], device=dev)
-    offset_t = torch.as_tensor(offset[seqs], device=dev)
-    base = torch.zeros((len(seqs), R), dtype=torch.int64, device=dev)
-    base[:, : R - 1] = draft.to(torch.int64)
-    other = (base + offset_t) % V
-    intended = torch.where(agree_t, base, other)
+    noise = normal((B, wl.rows, wl.vocab), wl.seed, f"loop_noise/{cycle}", dev)[seqs]
+    key16, offset = loop_plan(wl, cycle)
+    intended = loop_intended(wl, torch.as_tensor(key16[seqs], device=dev),
+                             torch.as_tensor(offset[seqs], device=dev), draft)
     top = noise.max(dim=-1, keepdim=True).values + 1.0
     noise.scatter_(-1, intended.unsqueeze(-1), top)
     return noise.to(dtype)

@@ -1,12 +1,15 @@
-"""GPU parity of the paged KV cache: injection and drafting through a page
-table must give exactly the contiguous cache's rows, drafts and logits (the
-contiguous path is pinned to the oracle elsewhere), wherever the pages sit in
-the pool; a missing page is a capacity error."""
+"""GPU parity of the paged KV cache against the oracle: the rows injected
+through a page table equal the oracle's K/V (RoPE at each row's position)
+within the activation tolerance, and the paged drafting pass gives the
+oracle's logits and drafts, wherever the pages sit in the pool. The paged
+results also equal the contiguous cache's bit for bit, and a missing page is
+a capacity error."""
 import numpy as np
 import pytest
 import torch
 
 import synth
+from oracle import dflash_ref as ref
 from tests import harness as H
 from tests.test_gpu_parity import SMALL
 
@@ -36,7 +39,7 @@ def page_view(dfl, wl, pages_per_seq, n_pages, seed, holes=()):
     return dfl.KvPages(k_pool, v_pool, t), table, k_pool, v_pool
 
 
-def fused_context(gd, lens):
+def fused_context(gd, lens, with_taps=False):
     wl = gd.wl
     total = int(sum(lens))
     taps = synth.taps(wl, total, "ctx", "cuda")
@@ -45,17 +48,29 @@ def fused_context(gd, lens):
     offs = np.concatenate([[0], np.cumsum(lens)])
     for b in range(len(lens)):
         h_pad[b, : lens[b]] = h[offs[b]:offs[b + 1]]
+    if with_taps:
+        return h_pad, [taps[offs[b]:offs[b + 1]] for b in range(len(lens))]
     return h_pad
+
+
+def oracle_context(gd, taps_b):
+    """The oracle's fused context and per-layer K/V of one sequence."""
+    oc = H.oracle_cfg(gd.wl)
+    n = taps_b.shape[0]
+    h_or = (ref.ctx_fuse(oc, gd.W["w_c"], gd.W["g_c"], taps_b.float().cpu()) if n
+            else np.zeros((0, gd.wl.d_model)))
+    kv = [ref.ctx_kv(oc, gd.W["w_qkv"][l], h_or, 0) for l in range(gd.wl.n_layers)]
+    return [k for k, _ in kv], [v for _, v in kv]
 
 
 @pytest.mark.parametrize("wl", [SMALL, synth.WORKLOADS["tiny_f32_L1_N128"].replace(batch=2)],
                          ids=["bf16_tcgen05", "fp32_simt"])
-def test_paged_cache_gives_the_contiguous_results_bit_for_bit(dfl, wl):
+def test_paged_cache_matches_the_oracle_and_the_contiguous_cache(dfl, wl):
     lens = [300, 45, 0][: wl.batch] if wl.batch == 3 else [200, 9]
     cap = 512
     gd = H.GpuDrafter(dfl, wl, max_rows=max(sum(lens), 16), ctx_capacity=cap)
     B = wl.batch
-    h_pad = fused_context(gd, lens)
+    h_pad, taps = fused_context(gd, lens, with_taps=True)
     gd.inject(h_pad, lens)
     n_new = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
     anchors = synth.anchors(wl)
@@ -63,6 +78,11 @@ def test_paged_cache_gives_the_contiguous_results_bit_for_bit(dfl, wl):
     draft_c, logits_c, _ = gd.draft(anchors, max(lens), want_logits=True)
     torch.cuda.synchronize()
     gd.check_status()
+    oc = H.oracle_cfg(wl)
+    want = []       # per sequence: the oracle's context K/V and its draft over them
+    for b in range(B):
+        kc, vc = oracle_context(gd, taps[b])
+        want.append((kc, vc, ref.draft_block(oc, gd.W, int(anchors[b]), kc, vc, lens[b])))
     for seed in (1, 2):   # two different placements of the pages in the pool
         pages, table, k_pool, v_pool = page_view(dfl, wl, cap // PAGE, B * cap // PAGE + 5, seed)
         ctx2 = torch.zeros(B, dtype=torch.int32, device="cuda")
@@ -71,9 +91,14 @@ def test_paged_cache_gives_the_contiguous_results_bit_for_bit(dfl, wl):
         gd.check_status()
         assert ctx2.cpu().tolist() == list(lens)
         for b in range(B):
+            kc, vc, _ = want[b]
             for p0 in range(0, lens[b], PAGE):
                 n = min(PAGE, lens[b] - p0)
                 pg = int(table[b, p0 // PAGE])
+                for l in range(wl.n_layers):
+                    # the page's rows against the oracle's K/V at positions p0 .. p0+n-1
+                    H.assert_act_close(k_pool[l, pg, :, :n], kc[l][:, p0:p0 + n], f"paged K l{l} b{b} p{p0}")
+                    H.assert_act_close(v_pool[l, pg, :, :n], vc[l][:, p0:p0 + n], f"paged V l{l} b{b} p{p0}")
                 assert torch.equal(k_pool[:, pg, :, :n], gd.k_cache[:, b, :, p0:p0 + n])
                 assert torch.equal(v_pool[:, pg, :, :n], gd.v_cache[:, b, :, p0:p0 + n])
         draft_p = torch.empty_like(draft_c)
@@ -82,6 +107,10 @@ def test_paged_cache_gives_the_contiguous_results_bit_for_bit(dfl, wl):
                                      logits=logits_p)
         torch.cuda.synchronize()
         gd.check_status()
+        for b in range(B):
+            out = want[b][2]
+            H.assert_logits_close(logits_p[b], out["logits"], f"paged logits b{b} placement {seed}")
+            H.assert_drafts_match(draft_p[b].cpu().numpy(), out["logits"], f"paged draft b{b} placement {seed}")
         assert torch.equal(draft_p, draft_c) and torch.equal(logits_p, logits_c)
 
 
