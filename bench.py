@@ -45,6 +45,13 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-next-rows", action="store_true",
                    help="skip the timing of the drafting variants (sampling, per-sequence gamma, unmasking)")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the other workloads, the prefill and the draft-verify loop")
+    p.add_argument("--mode", choices=["step", "prefill", "loop"], default="step",
+                   help="step: the drafting cycle (default, full JSON line); prefill: context fusion + "
+                        "injection of a long prefill only; loop: the draft-verify loop workload only")
+    p.add_argument("--prefill-rows", type=int, default=0,
+                   help="--mode prefill: tokens of the prefill (default: the workload's context)")
     return p.parse_args()
 
 
@@ -331,8 +338,15 @@ def measure_variant(cyc: DraftCycle, fn, steps: int, tokens: int, peak_gbs: floa
             "frac_of_hbm": round(gbs / peak_gbs, 4), "steps": steps}
 
 
-def kernel_roofline(cyc: DraftCycle, peak_gbs: float, reps: int = 5):
-    """Per-kind algorithmic bytes / CUDA-event time over traced steps."""
+def kernel_roofline(cyc: DraftCycle, peak_gbs: float, step_ms: float, reps: int = 5):
+    """Per-kind algorithmic bytes / time over traced steps.
+
+    A traced step launches its kernels one at a time between CUDA events, so
+    each kind's event time is its serialised time; inside the graph-replayed
+    step, programmatic dependent launch overlaps each kernel's start with its
+    predecessor's tail and the sum is shorter. Each kind's time within the
+    step is its share of the serialised sum times the measured step time
+    (step_ms), so that the kinds add up to the step; both are reported."""
     dfl = cyc.dfl
     rec = dfl.TraceRecorder(512)
     agg = {}
@@ -347,12 +361,16 @@ def kernel_roofline(cyc: DraftCycle, peak_gbs: float, reps: int = 5):
             a[3] += 1
     names = {dfl.K_GEMM: "gemm_tc", dfl.K_ATTN: "attention", dfl.K_NORM: "row_kernels",
              dfl.K_ARGMAX: "argmax", dfl.K_VERIFY: "verify"}
+    serial = sum(a[2] for a in agg.values()) / reps
+    scale = min(1.0, step_ms / serial) if serial > 0 else 1.0
     out = {}
     for kind, (b, fl, ms, n) in agg.items():
-        gbs = b / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+        ms_in = ms / reps * scale          # this kind's time within one graph-replayed step
+        gbs = b / reps / (ms_in * 1e-3) / 1e9 if ms_in > 0 else 0.0
         out[names.get(kind, str(kind))] = {
-            "launches_per_step": n // reps, "ms_per_step": ms / reps, "bytes_per_launch": b / n,
-            "achieved_gbs": gbs, "frac_of_hbm": gbs / peak_gbs, "tflops": fl / (ms * 1e-3) / 1e12 if ms > 0 else 0.0}
+            "launches_per_step": n // reps, "ms_per_step": ms_in, "serialised_ms_per_step": ms / reps,
+            "bytes_per_launch": b / n, "achieved_gbs": gbs, "frac_of_hbm": gbs / peak_gbs,
+            "tflops": fl / reps / (ms_in * 1e-3) / 1e12 if ms_in > 0 else 0.0}
     return out
 
 
@@ -392,6 +410,211 @@ def long_context_attention(dfl, dev, peak_gbs: float, reps: int = 10) -> dict:
     del cyc
     torch.cuda.empty_cache()
     return out
+
+
+def prefill_row(dfl, wl: synth.Workload, W: dict, dev, T: int, tf_peak: float, reps: int) -> dict:
+    """Context fusion + injection of a T-token prefill of one sequence (the
+    context feature is computed once per position and cached, then reused by
+    every drafting step): tokens along the GEMM's A rows, 128 x 256 tcgen05
+    tiles, tensor-bound. Each call is timed on its own with CUDA events on the
+    launching stream (fusion: the W_c GEMM and the norm pass; injection: the
+    K|V GEMM of all layers and the length update); the GEMM launches alone are
+    timed from one traced run."""
+    R = wl.rows
+    cfg = dfl.config_from_workload(wl, max_batch=1, ctx_capacity=(T + R + 127) // 128 * 128)
+    w = dfl.Weights(cfg, W, dev)
+    ws = dfl.Workspace(cfg, T, dev)
+    dt = synth.torch_dtype(wl.dtype)
+    taps = synth.taps(wl, T, f"prefill{T}", dev)
+    h = torch.empty((1, T, wl.d_model), dtype=dt, device=dev)
+    shape = (wl.n_layers, 1, wl.n_kv_heads, cfg.ctx_capacity, wl.head_dim)
+    k_cache = torch.zeros(shape, dtype=dt, device=dev)
+    v_cache = torch.zeros(shape, dtype=dt, device=dev)
+    ctx_len = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_new = torch.full((1,), T, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fuse(trace=None):
+        dfl.dflash_ctx_fuse(cfg, w, taps, h[0], ws, trace=trace)
+
+    def inject(trace=None):
+        ctx_len.zero_()
+        dfl.dflash_kv_inject(cfg, w, h, n_new, ctx_len, k_cache, v_cache, status, ws, trace=trace)
+
+    for _ in range(2):
+        fuse()
+        inject()
+    torch.cuda.synchronize()
+    fuse_ms = time_steps(fuse, reps, stream) / reps
+    inject_ms = time_steps(inject, reps, stream) / reps
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"prefill: device status {st}: {dfl.status_string(st)}")
+    rec = dfl.TraceRecorder(16)
+    gemm = {}
+    for name, fn in (("fuse", fuse), ("inject", inject)):
+        ms = fl = 0.0
+        for _ in range(reps):
+            rec.reset()
+            fn(trace=rec.struct)
+            for kind, _, f, t in rec.records():
+                if kind == dfl.K_GEMM:
+                    ms += t
+                    fl += f
+        gemm[name] = (ms / reps, fl / reps)
+    K = wl.n_taps * wl.d_target
+    fpl = 2 * wl.n_kv_heads * wl.head_dim
+    flops = 2.0 * T * wl.d_model * K + 2.0 * T * wl.n_layers * fpl * wl.d_model
+    tot_ms = fuse_ms + inject_ms
+    g_ms = gemm["fuse"][0] + gemm["inject"][0]
+    g_fl = gemm["fuse"][1] + gemm["inject"][1]
+    out = {"tokens": T, "layers": wl.n_layers, "fuse_us": round(fuse_ms * 1e3, 1),
+           "inject_us": round(inject_ms * 1e3, 1), "us": round(tot_ms * 1e3, 1),
+           "gflop": round(flops / 1e9, 1), "tflops": round(flops / (tot_ms * 1e-3) / 1e12, 1),
+           "frac_of_bf16_peak": round(flops / (tot_ms * 1e-3) / 1e12 / tf_peak, 4),
+           "gemm_fuse_us": round(gemm["fuse"][0] * 1e3, 1), "gemm_inject_us": round(gemm["inject"][0] * 1e3, 1),
+           "gemm_tflops": round(g_fl / (g_ms * 1e-3) / 1e12, 1) if g_ms > 0 else None,
+           "gemm_frac_of_bf16_peak": round(g_fl / (g_ms * 1e-3) / 1e12 / tf_peak, 4) if g_ms > 0 else None,
+           "floor_us": round(flops / (tf_peak * 1e12) * 1e6, 1),
+           "what": f"context fusion (W_c over {wl.n_taps} taps) + K/V injection of all {wl.n_layers} layers "
+                   f"for a {T}-token prefill; calls timed with CUDA events; peak = measured bf16 burst"}
+    del taps, h, k_cache, v_cache, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+class LoopRun:
+    """The full draft-verify loop: every cycle drafts a block over each
+    sequence's context, the synthetic target verifies it (greedy
+    accept), and the tapped states of the tau accepted positions are fused
+    and injected, so the context grows by tau; the next anchor comes from
+    verification. Nothing goes through the host between cycles: the whole
+    loop is one CUDA graph.
+
+    The target's logits are synthetic (synth.loop_target_logits): per cycle a
+    resident N(0,1) noise tensor, in which the token the target picks for each
+    row gets the row max + 1 before verification and its old value back after
+    it (a few small torch kernels per cycle, inside the timed region). The
+    target agrees with a drafted token with probability 0.8, decided by a
+    hash of the token itself, so E[tau] = 1 + sum_k 0.8^k = 4.89."""
+
+    def __init__(self, dfl, wl: synth.Workload, dev):
+        self.dfl, self.wl, self.dev = dfl, wl, dev
+        B, R, V, D = wl.batch, wl.rows, wl.vocab, wl.d_model
+        self.cfg = dfl.config_from_workload(wl)
+        self.W = synth.weights(wl, dev)
+        self.w = dfl.Weights(self.cfg, self.W, dev)
+        self.ws = dfl.Workspace(self.cfg, max(wl.ctx * B, B * R, 16), dev)
+        dt = synth.torch_dtype(wl.dtype)
+        shape = (wl.n_layers, B, wl.n_kv_heads, self.cfg.ctx_capacity, wl.head_dim)
+        self.k_cache = torch.zeros(shape, dtype=dt, device=dev)
+        self.v_cache = torch.zeros(shape, dtype=dt, device=dev)
+        self.ctx_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # prefill of every sequence's context (set-up, not timed)
+        taps = synth.taps(wl, B * wl.ctx, "prefill", dev).view(B, wl.ctx, -1)
+        h = torch.empty((B, wl.ctx, D), dtype=dt, device=dev)
+        for b in range(B):
+            dfl.dflash_ctx_fuse(self.cfg, self.w, taps[b], h[b], self.ws)
+        dfl.dflash_kv_inject(self.cfg, self.w, h, torch.full((B,), wl.ctx, dtype=torch.int32, device=dev),
+                             self.ctx_len, self.k_cache, self.v_cache, self.status, self.ws)
+        del taps, h
+        self.ctx0 = self.ctx_len.clone()
+        # per-cycle inputs: tapped states of the block's positions, the
+        # target's noise and row maxima, the agreement keys
+        self.taps = [synth.taps(wl, B * R, f"loop{c}", dev) for c in range(wl.cycles)]
+        self.noise = [synth.normal((B, R, V), wl.seed, f"loop_noise/{c}", dev) for c in range(wl.cycles)]
+        self.top = [n.max(dim=-1, keepdim=True).values + 1.0 for n in self.noise]
+        plans = [synth.loop_plan(wl, c) for c in range(wl.cycles)]
+        self.key16 = torch.as_tensor(np.stack([p[0] for p in plans]), device=dev)
+        self.offset = torch.as_tensor(np.stack([p[1] for p in plans]), device=dev)
+        self.anchor0 = torch.as_tensor(synth.anchors(wl), device=dev)
+        self.anchor = self.anchor0.clone()
+        self.draft = torch.empty((B, wl.gamma), dtype=torch.int32, device=dev)
+        self.tau = torch.empty(B, dtype=torch.int32, device=dev)
+        self.committed = torch.empty((B, R), dtype=torch.int32, device=dev)
+        self.next_anchor = torch.empty(B, dtype=torch.int32, device=dev)
+        self.h_new = torch.empty((B, R, D), dtype=dt, device=dev)
+        self.taus = torch.zeros((wl.cycles, B), dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+
+    def cycle(self, c: int):
+        d, wl, cfg = self.dfl, self.wl, self.cfg
+        hint = wl.ctx + c * wl.rows          # ctx_len[b] <= ctx + c * R before cycle c
+        d.dflash_draft_block(cfg, self.w, self.anchor, self.ctx_len, hint, self.k_cache, self.v_cache,
+                             self.draft, self.status, self.ws)
+        idx = synth.loop_intended(wl, self.key16[c], self.offset[c], self.draft).unsqueeze(-1)
+        logits = self.noise[c]
+        saved = logits.gather(-1, idx)
+        logits.scatter_(-1, idx, self.top[c])
+        d.dflash_verify_accept(cfg, logits, self.draft, self.tau, self.committed, self.next_anchor, self.ws)
+        logits.scatter_(-1, idx, saved)
+        d.dflash_ctx_fuse(cfg, self.w, self.taps[c], self.h_new.view(-1, wl.d_model), self.ws)
+        d.dflash_kv_inject(cfg, self.w, self.h_new, self.tau, self.ctx_len, self.k_cache, self.v_cache,
+                           self.status, self.ws)
+        self.anchor.copy_(self.next_anchor)
+        self.taus[c].copy_(self.tau)
+
+    def run(self):
+        self.ctx_len.copy_(self.ctx0)
+        self.anchor.copy_(self.anchor0)
+        for c in range(self.wl.cycles):
+            self.cycle(c)
+
+
+def measure_loop(dfl, wl: synth.Workload, dev, reps: int, peak_gbs: float) -> dict:
+    lr = LoopRun(dfl, wl, dev)
+    lr.run()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        lr.run()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lr.run()
+    g.replay()
+    torch.cuda.synchronize()
+    ms = time_steps(g.replay, reps, torch.cuda.current_stream()) / reps
+    st = int(lr.status.item())
+    if st != 0:
+        raise RuntimeError(f"loop: device status {st}: {dfl.status_string(st)}")
+    taus = lr.taus.cpu().numpy()
+    committed = int(taus.sum())
+    B, C = wl.batch, wl.cycles
+    out = {"workload": wl.name, "cycles": C, "batch": B, "loop_ms": round(ms, 2),
+           "us_per_cycle": round(1e3 * ms / C, 1), "mean_tau": round(float(taus.mean()), 4),
+           "committed_tokens": committed, "committed_tok_s": round(committed / (ms * 1e-3), 1),
+           "drafted_tok_s": round(C * B * wl.gamma / (ms * 1e-3), 1),
+           "final_context": lr.ctx_len.cpu().tolist(), "replays": reps,
+           "what": "draft -> greedy verify -> fusion + injection of the tau accepted positions, every "
+                   "cycle on the device, the whole loop one CUDA graph; synthetic target agreeing with a "
+                   "drafted token with probability 0.8 (E[tau] = 4.89); its per-cycle logit edits (a few "
+                   "small torch kernels) are inside the timed region"}
+    del g, lr
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_workload(dfl, wl: synth.Workload, dev, steps: int, peak_gbs: float) -> dict:
+    """One drafting cycle of another workload, graph-replayed like the headline."""
+    cyc = DraftCycle(dfl, wl, dev)
+    for _ in range(3):
+        cyc.step()
+    r = measure_variant(cyc, cyc.step, steps, wl.batch * wl.gamma, peak_gbs)
+    kern = kernel_roofline(cyc, peak_gbs, r["us_per_step"] * 1e-3, reps=2)
+    r["gemm_frac_of_hbm"] = round(kern.get("gemm_tc", {}).get("frac_of_hbm", 0.0), 4)
+    r["attention_frac_of_hbm"] = round(kern.get("attention", {}).get("frac_of_hbm", 0.0), 4)
+    r["gemm_tflops"] = round(kern.get("gemm_tc", {}).get("tflops", 0.0), 1)
+    r["workload"] = wl.name
+    st = int(cyc.status.item())
+    if st != 0:
+        raise RuntimeError(f"{wl.name}: device status {st}: {dfl.status_string(st)}")
+    del cyc
+    torch.cuda.empty_cache()
+    return r
 
 
 class OracleCycle:
@@ -580,7 +803,7 @@ def run_gpu(args):
     d2h = o_out.numel() * 4
 
     launches = cyc.launches_per_step()
-    kern = kernel_roofline(cyc, hbm)
+    kern = kernel_roofline(cyc, hbm, ms / args.steps)
     g = kern.get("gemm_tc", {})
     traffic = traffic_from_profile("gemm.cu", f"gemm_tc_{args.workload}.md")
     roof = {"kernel": "gemm_tc (every projection launch of a step: QKV, O, gate|up, down, LM head, "
@@ -605,6 +828,16 @@ def run_gpu(args):
         }
         if wl.dtype == "bf16":
             next_rows["attention_context_32k"] = long_context_attention(dfl, dev, hbm)
+    extra = None
+    if rank == 0 and not args.no_extra and wl.dtype == "bf16":
+        extra = {}
+        for T, reps in ((wl.ctx, 10), (32768, 3)):
+            extra[f"prefill_{T}"] = prefill_row(dfl, wl, cyc.W, dev, T, tf_burst, reps)
+        lwl = synth.WORKLOADS["qwen3_8b_L8_loop_B4"]
+        extra["loop_" + lwl.name] = measure_loop(dfl, lwl, dev, 3, hbm)
+        for name in ("tiny_f32_L1_N128", "qwen3_8b_L5_N32768_B1", "qwen3_8b_L5_ragged_B16"):
+            if name != wl.name:
+                extra[name] = measure_workload(dfl, synth.WORKLOADS[name], dev, min(args.steps, 20), hbm)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
@@ -634,6 +867,7 @@ def run_gpu(args):
                         for k, v in kern.items()},
             "cpu_baseline": cpu,
             "next_rows": next_rows,
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -677,10 +911,29 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0}}), flush=True)
 
 
+def run_mode(args):
+    """--mode prefill / loop: one measurement alone (profiling captures)."""
+    dev = "cuda:0"
+    torch.cuda.set_device(dev)
+    import block_diffusion_drafter_gb300 as dfl
+    dfl.load()
+    wl = synth.WORKLOADS[args.workload]
+    hbm, tf_burst, _, _ = measured_peaks()
+    if args.mode == "prefill":
+        T = args.prefill_rows or wl.ctx
+        out = prefill_row(dfl, wl, synth.weights(wl, dev), dev, T, tf_burst, max(args.steps, 1))
+    else:
+        lwl = wl if wl.cycles > 0 else synth.WORKLOADS["qwen3_8b_L8_loop_B4"]
+        out = measure_loop(dfl, lwl, dev, max(args.steps, 1), hbm)
+    print(json.dumps({"mode": args.mode, "workload": wl.name, **out}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.mode != "step":
+        run_mode(args)
     else:
         run_gpu(args)
 
