@@ -232,6 +232,7 @@ namespace {
 
 void fill_from_plan(GemmArgs& g, const GemmPlan& p, int k) {
   g.k = k;
+  g.group_m = p.group_m;
   g.bn = p.bn;
   g.n_sub = p.n_sub;
   g.kt_per_split = p.kt_per_split;
@@ -320,14 +321,14 @@ dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, fl
   GemmPlan plan;
   const bool swap = M <= kMaxBN;
   if (swap) {
-    plan = plan_gemm((N + kBM - 1) / kBM, M, K, es, cx.sms, true);
+    plan = plan_gemm((N + kBM - 1) / kBM, M, K, es, cx.sms, true, true);
     if (!make_operand_map(&amap, w, es, K, N, 1, kBM) ||
         !make_operand_map(&bmap, x, es, K, M, 1, plan.bn / plan.n_sub))
       return DFLASH_ERR_ALIGN;
     g.swap = 1;
     g.a_weights = 1;
   } else {
-    plan = plan_gemm((M + kBM - 1) / kBM, N, K, es, cx.sms, false);
+    plan = plan_gemm((M + kBM - 1) / kBM, N, K, es, cx.sms, false, false);
     if (!make_operand_map(&amap, x, es, K, M, 1, kBM) ||
         !make_operand_map(&bmap, w, es, K, N, 1, plan.bn / plan.n_sub))
       return DFLASH_ERR_ALIGN;
@@ -366,14 +367,14 @@ dflash_status dflash_ctx_fuse(const dflash_config* c, const dflash_weights* w, c
   GemmPlan plan;
   const bool swap = T <= kMaxBN;
   if (swap) {
-    plan = plan_gemm(D / kBM, T, K, es, cx.sms, true);
+    plan = plan_gemm(D / kBM, T, K, es, cx.sms, true, true);
     if (!make_operand_map(&amap, w->w_c, es, K, D, 1, kBM) ||
         !make_operand_map(&bmap, taps, es, K, T, 1, plan.bn / plan.n_sub))
       return DFLASH_ERR_ALIGN;
     g.swap = 1;
     g.a_weights = 1;
   } else {
-    plan = plan_gemm((T + kBM - 1) / kBM, D, K, es, cx.sms, false);
+    plan = plan_gemm((T + kBM - 1) / kBM, D, K, es, cx.sms, false, false);
     if (!make_operand_map(&amap, taps, es, K, T, 1, kBM) ||
         !make_operand_map(&bmap, w->w_c, es, K, D, 1, plan.bn / plan.n_sub))
       return DFLASH_ERR_ALIGN;
@@ -432,7 +433,7 @@ static dflash_status kv_inject_impl(const dflash_config* c, const dflash_weights
   GemmPlan plan;
   const bool swap = rows <= kMaxBN;
   if (swap) {
-    plan = plan_gemm(c->n_layers * fpl / kBM, rows, D, es, cx.sms, true);
+    plan = plan_gemm(c->n_layers * fpl / kBM, rows, D, es, cx.sms, true, true);
     if (!make_operand_map(&amap, w->w_qkv, es, D, nqkv, c->n_layers, kBM) ||
         !make_operand_map(&bmap, h_ctx, es, D, rows, 1, plan.bn / plan.n_sub))
       return DFLASH_ERR_ALIGN;
@@ -443,7 +444,7 @@ static dflash_status kv_inject_impl(const dflash_config* c, const dflash_weights
   } else {
     // feature tiles must not straddle layers
     const int cap = fpl % 512 == 0 ? 512 : (fpl % 256 == 0 ? 256 : kBM);
-    plan = plan_gemm((rows + kBM - 1) / kBM, c->n_layers * fpl, D, es, cx.sms, false, cap);
+    plan = plan_gemm((rows + kBM - 1) / kBM, c->n_layers * fpl, D, es, cx.sms, false, false, cap);
     if (!make_operand_map(&amap, h_ctx, es, D, rows, 1, kBM) ||
         !make_operand_map(&bmap, w->w_qkv, es, D, nqkv, c->n_layers, plan.bn / plan.n_sub))
       return DFLASH_ERR_ALIGN;
@@ -548,15 +549,15 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
   const bool split = bf16 != 0;
   const int rows_max = c->max_batch * R, nmask_max = c->max_batch * c->gamma;
   const int parts = split ? 2 : 1;
-  GemmPlan p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, kMaxBN, split);
-  const GemmPlan p_o = plan_gemm(D / kBM, rows, HD, es, cx.sms, true, kMaxBN, split);
-  GemmPlan p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, kMaxBN, split);
+  GemmPlan p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, true, kMaxBN, split);
+  const GemmPlan p_o = plan_gemm(D / kBM, rows, HD, es, cx.sms, true, true, kMaxBN, split);
+  GemmPlan p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, true, kMaxBN, split);
   if (p_qkv.b_split != p_gu.b_split) {  // both read the same normed activations
-    p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, kMaxBN, false);
-    p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, kMaxBN, false);
+    p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, true, kMaxBN, false);
+    p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, true, kMaxBN, false);
   }
-  const GemmPlan p_dn = plan_gemm(D / kBM, rows, F, es, cx.sms, true, kMaxBN, split);
-  const GemmPlan p_lm = plan_gemm((V + kBM - 1) / kBM, nmask, D, es, cx.sms, false, kMaxBN, split);
+  const GemmPlan p_dn = plan_gemm(D / kBM, rows, F, es, cx.sms, true, true, kMaxBN, split);
+  const GemmPlan p_lm = plan_gemm((V + kBM - 1) / kBM, nmask, D, es, cx.sms, false, true, kMaxBN, split);
 
   // B boxes bring the valid token rows alone (hi and lo rows when the plan
   // packs split operands) when one box spans the tile

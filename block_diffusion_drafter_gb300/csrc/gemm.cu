@@ -426,6 +426,26 @@ struct SmemHeader {
 
 static_assert(sizeof(SmemHeader) + 1023 <= kSmemHeaderBytes, "shared-memory header allowance");
 
+// Tile (m_tile, n_tile) of grid index t. Decode orientation (A = weights):
+// n_tile fastest, so the CTAs that share a weight tile are adjacent in launch
+// order and read it from HBM once. Token-major orientation (B = weights):
+// groups of group_m token tiles, m fastest inside a group, so the CTAs of a
+// wave share a few token tiles and a band of weight tiles instead of
+// re-streaming either operand for every tile of the other.
+__device__ __forceinline__ void tile_of(const GemmArgs& g, int t, int& m, int& n) {
+  if (g.swap || g.group_m <= 0) {
+    n = t % g.n_tiles;
+    m = t / g.n_tiles;
+    return;
+  }
+  const int per_group = g.group_m * g.n_tiles;
+  const int grp = t / per_group, first = grp * g.group_m;
+  const int gm = min(g.group_m, g.m_tiles - first);
+  const int r = t - grp * per_group;
+  m = first + r % gm;
+  n = r / gm;
+}
+
 // One instantiation per (operand type, split activations, epilogue op), so
 // that each launch runs only the code of its own case.
 template <bool kTF32, bool kSplit, int kOp, bool kWide>
@@ -440,7 +460,9 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
 
   constexpr int kBK = kTF32 ? 32 : 64;  // 128 bytes of k per row either way
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x, split = blockIdx.y, n_tile = blockIdx.z;
+  const int split = blockIdx.y;
+  int m_tile, n_tile;
+  tile_of(g, blockIdx.x, m_tile, n_tile);
   int issued = 0;  // producer: k-steps whose TMA loads were issued
   const int KT = g.k / kBK;
   const int kt0 = split * g.kt_per_split;
@@ -741,7 +763,7 @@ bool make_operand_map(CUtensorMap* map, const void* base, int elem_bytes, uint64
 }
 
 GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
-                   int bn_cap, bool b_split) {
+                   bool weights_a, int bn_cap, bool b_split) {
   GemmPlan p{};
   const int bk = 128 / elem_bytes;
   const int KT = k / bk;
@@ -750,31 +772,54 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   b_split = b_split && 2 * n_rows <= (bn_cap < 256 ? bn_cap : 256);
   const int n16 = ((b_split ? 2 * n_rows : n_rows) + 15) / 16 * 16;
   const int cap1 = bn_cap < 256 ? bn_cap : 256;
+  // Two B tiles of at most 256 rows rather than one tile of up to 512 rows
+  // (two MMAs): an accumulator of <= 256 TMEM columns leaves room for a
+  // second CTA on the SM, whose main loop then runs while this one's
+  // epilogue drains. Decode: two halves of the tokens (the weight tile is
+  // read twice, the second time from L2, as the two CTAs are adjacent in
+  // launch order); token-major: 256-feature tiles.
+  bool one_wide = false;
+  if (const char* e = getenv("DFLASH_GEMM_ONE_WIDE_TILE")) one_wide = atoi(e) != 0;   // tuning override
   if (n16 <= cap1) {
     p.bn = n16; p.n_sub = 1; p.n_tiles = 1;
-  } else if (n16 <= bn_cap && n16 <= kMaxBN) {
+  } else if (n16 <= bn_cap && n16 <= kMaxBN && one_wide) {
     p.bn = (n_rows + 31) / 32 * 32; p.n_sub = 2; p.n_tiles = 1;
+  } else if (n16 <= bn_cap && n16 <= kMaxBN && weights_a) {
+    p.bn = ((n_rows + 1) / 2 + 15) / 16 * 16; p.n_sub = 1; p.n_tiles = 2;
   } else {
     p.bn = cap1; p.n_sub = 1; p.n_tiles = (n_rows + cap1 - 1) / cap1;
   }
   p.m_tiles = m_tiles;
-  // Weight streaming wants many resident CTAs more than deep pipelines: a
-  // short ring (3 stages) leaves room for 3 CTAs per SM on the skinny
-  // shapes, whose prologue/epilogue then overlap other CTAs' streaming.
+  p.group_m = 0;
+  if (!weights_a) {
+    p.group_m = 8;
+    if (const char* e = getenv("DFLASH_GEMM_GROUP_M")) p.group_m = atoi(e);   // tuning override
+  }
   p.b_split = b_split ? 1 : 0;
+  // Resident CTAs per SM follow from the accumulator's TMEM columns (512 per
+  // SM): narrow tiles (a few tokens) keep three CTAs per SM with a short
+  // ring (3 stages), whose prologues and epilogues then overlap the others'
+  // streaming; a 256-column accumulator two CTAs, a 512-column one a single
+  // CTA; the ring takes what shared memory that leaves.
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(p.bn)) tmem_cols <<= 1;
   const size_t stage = 16384 + static_cast<size_t>(p.bn) * 128;
   const size_t staging = static_cast<size_t>(p.bn < kBM ? p.bn : kBM) * 129 * 4;
-  int stages = p.bn <= 128 ? 3 : static_cast<int>((222 * 1024 - kSmemHeaderBytes) / stage);
+  int target = p.bn <= 128 ? 3 : static_cast<int>(512 / tmem_cols);
+  if (const char* e = getenv("DFLASH_GEMM_CTAS")) target = atoi(e);   // tuning override
+  if (target < 1) target = 1;
+  size_t per_cta = static_cast<size_t>(233472 / target) - 1024;
+  if (per_cta > 232448) per_cta = 232448;
+  int stages = p.bn <= 128 ? 3 : static_cast<int>((per_cta - kSmemHeaderBytes) / stage);
   if (const char* e = getenv("DFLASH_GEMM_STAGES")) stages = atoi(e);   // tuning override
   if (stages > 16) stages = 16;
   if (stages > KT && KT >= 2) stages = KT;
   if (stages < 2) stages = 2;
   while (static_cast<size_t>(stages) * stage < staging) ++stages;
+  while (stages > 2 && kSmemHeaderBytes + static_cast<size_t>(stages) * stage > 232448) --stages;
   p.stages = stages;
   p.smem_bytes = kSmemHeaderBytes + static_cast<size_t>(stages) * stage;
   // resident CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and TMEM
-  uint32_t tmem_cols = 32;
-  while (tmem_cols < static_cast<uint32_t>(p.bn)) tmem_cols <<= 1;
   int ctas_per_sm = static_cast<int>(233472 / (p.smem_bytes + 1024));
   if (ctas_per_sm > 4) ctas_per_sm = 4;
   while (ctas_per_sm > 1 && ctas_per_sm * tmem_cols > 512) --ctas_per_sm;
@@ -803,7 +848,7 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   // without split-K the epilogue drains 128 columns at a time, and a packed
   // tile must pair each token's hi and lo columns inside one drain
   if (b_split && p.splits == 1 && p.bn > kBM)
-    return plan_gemm(m_tiles, n_rows, k, elem_bytes, num_sms, allow_split, bn_cap, false);
+    return plan_gemm(m_tiles, n_rows, k, elem_bytes, num_sms, allow_split, weights_a, bn_cap, false);
   return p;
 }
 
@@ -864,7 +909,7 @@ cudaError_t launch_gemm(const CUtensorMap& a_map, const CUtensorMap& b_map, cons
     done = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.m_tiles, plan.splits, plan.n_tiles);
+  cfg.gridDim = dim3(plan.m_tiles * plan.n_tiles, plan.splits, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = stream;

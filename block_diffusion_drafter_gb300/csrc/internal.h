@@ -101,6 +101,7 @@ struct GemmArgs {
   int b_box_rows;     // rows per B box of the tensor map (0: bn / n_sub); rows of a tile
                       // past the box are never loaded and feed only unused accumulator columns
   int swap;           // 1: A rows are output features and B rows tokens; 0: the reverse
+  int group_m;        // token-major tiles: grid order in groups of group_m A tiles (0: n fastest)
   int a_weights;      // 1: A is a weight (independent of earlier kernels): prefetch before PDL wait
   int tf32;           // 1: fp32 operands through kind::tf32
   int* dev_status;
@@ -109,14 +110,16 @@ struct GemmArgs {
 
 struct GemmPlan {
   int bn, n_sub, splits, kt_per_split, m_tiles, n_tiles, stages;
+  int group_m;        // grid order (GemmArgs::group_m)
   int b_split;        // B tile packs hi and lo rows (bn covers 2 n_rows)
   size_t smem_bytes;
 };
 
-// Chooses tile shape, split count and pipeline depth for m_tiles A tiles
-// against n_rows B rows over k (elements of elem_bytes each).
+// Chooses tile shape, split count, pipeline depth and grid order for
+// m_tiles A tiles against n_rows B rows over k (elements of elem_bytes each);
+// weights_a: A is the weight matrix (decode orientation), else B is.
 GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
-                   int bn_cap = kMaxBN, bool b_split = false);
+                   bool weights_a, int bn_cap = kMaxBN, bool b_split = false);
 
 // Builds a 3-D tensor map over a [z][rows][k] row-major operand with a box of
 // (64 or 32 elements of k) x box_rows x 1 and 128-byte swizzle.

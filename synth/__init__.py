@@ -94,6 +94,11 @@ WORKLOADS = {
     # split-KV attention over 32K keys
     "qwen3_8b_L1_N32768_B1": Workload(
         "qwen3_8b_L1_N32768_B1", n_layers=1, batch=1, ctx=32768, seed=1007, **_QWEN3_8B),
+    # one-layer version of the ragged batch-16 case, for kernel-level profiler
+    # captures of the batched projections
+    "qwen3_8b_L1_ragged_B16": Workload(
+        "qwen3_8b_L1_ragged_B16", n_layers=1, batch=16, ctx=8192, ctx_min=512,
+        seed=1004, **_QWEN3_8B),
     # full draft-verify loop: 8 layers, batch 4, context 4096, 256 cycles
     "qwen3_8b_L8_loop_B4": Workload(
         "qwen3_8b_L8_loop_B4", n_layers=8, batch=4, ctx=4096, cycles=256,
