@@ -408,6 +408,156 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
   }
 }
 
+// ---------------------------------------------------------------- token-major epilogue
+// Tokens along A rows (context fusion and injection of a prefill, plain
+// projections): TMEM lane = token, column = output feature, so every thread
+// owns one token's row of the accumulator and finishes it alone -- 16
+// columns per tcgen05.ld, no staging through shared memory, no barrier. The
+// global accesses of a thread are 16 consecutive features (64-byte fp32 or
+// 32-byte bf16 vectors), and its loads of a batch (RoPE table rows) are all
+// issued before they are used.
+template <int kOp>
+__host__ __device__ constexpr bool token_major_direct() {
+  return kOp == EPI_STORE || kOp == EPI_FUSE || kOp == EPI_KV;
+}
+
+__device__ __forceinline__ void store16(void* out, int bf16, size_t idx, const float* v) {
+  if (bf16) {
+    uint4 w[2];
+    uint32_t* u = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      u[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + idx);
+    d[0] = w[0];
+    d[1] = w[1];
+  } else {
+    float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+__device__ __forceinline__ void store8(void* out, int bf16, size_t idx, const float* v) {
+  if (bf16) {
+    uint4 w;
+    uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      u[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + idx) = w;
+  } else {
+    float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + idx);
+    d[0] = make_float4(v[0], v[1], v[2], v[3]);
+    d[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+template <int kOp>
+__device__ void epilogue_token_major(const GemmArgs& g, uint32_t t_lane, int tok, int n_tile) {
+  const Epi& e = g.epi;
+  const bool live = tok < e.n_tok;
+  const int f0 = n_tile * g.bn;  // first feature of the tile
+  if (kOp == EPI_STORE || kOp == EPI_FUSE) {
+    // vector stores need whole, 16-element-aligned runs of features
+    const bool vec = (e.ld % 16) == 0 && (f0 % 16) == 0;
+    float ss = 0.f;
+    for (int j = 0; j < g.bn; j += 16) {
+      float v[16];
+      tmem_ld16(t_lane + j, v);
+      tmem_ld_wait();
+      const int f = f0 + j;
+      if (kOp == EPI_FUSE) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss += v[i] * v[i];
+      }
+      if (live) {
+        const size_t o = static_cast<size_t>(tok) * e.ld + f;
+        if (vec && f + 16 <= e.n_feat) {
+          store16(e.out, kOp == EPI_FUSE ? 0 : e.out_bf16, o, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (f + i < e.n_feat) store_out(e.out, kOp == EPI_FUSE ? 0 : e.out_bf16, o + i, v[i]);
+        }
+      }
+      if (kOp == EPI_FUSE && ((j + 16) % kBM) == 0) {
+        // one slot per 128-feature group, summed in ascending feature order
+        if (live && f + 16 <= e.n_feat)
+          e.row_ss[static_cast<size_t>(tok) * e.n_ss + (f + 16) / kBM - 1] = ss;
+        ss = 0.f;
+      }
+    }
+    return;
+  }
+  // EPI_KV: feature gf of the tile is [K heads ; V heads] of layer gf / fpl.
+  // The tile holds whole 128-feature groups (the launcher checks), so a head
+  // and its RoPE partner columns d and d + Dh/2 are in the same tile.
+  const int Dh = e.head_dim, half = Dh >> 1;
+  const int nk = e.n_kv_heads * Dh;
+  int pos = -1, seq = 0;
+  if (live) {
+    seq = tok / e.rows_per_seq;
+    const int t = tok - seq * e.rows_per_seq;
+    const int base = e.ctx_len[seq], nn = e.n_new[seq];
+    if (t < nn && base + nn <= e.ncap - e.reserve) pos = base + t;
+    if (pos >= 0 && e.page_table != nullptr) {
+      const int pg = e.page_table[static_cast<size_t>(seq) * e.pages_per_seq + pos / kPageKeys];
+      if (pg < 0 || pg >= e.n_pages) {
+        report(g.dev_status, DFLASH_ERR_CAPACITY);
+        pos = -1;
+      } else {
+        seq = pg;
+      }
+    }
+  }
+  for (int h0 = 0; h0 < g.bn; h0 += Dh) {   // one head of K or V per step
+    const int gf = f0 + h0;
+    const int layer = gf / e.feat_per_layer;
+    const int f = gf - layer * e.feat_per_layer;   // position within [K heads ; V heads]
+    const bool is_k = f < nk;
+    const int head = (is_k ? f : f - nk) / Dh;
+    void* dst = is_k ? e.k_cache : e.v_cache;
+    const size_t row = e.page_table != nullptr
+                           ? ((static_cast<size_t>(layer) * e.n_pages + seq) * e.n_kv_heads + head) * kPageKeys +
+                                 (pos >= 0 ? pos % kPageKeys : 0)
+                           : ((static_cast<size_t>(layer) * e.max_batch + seq) * e.n_kv_heads + head) * e.ncap +
+                                 (pos >= 0 ? pos : 0);
+    const bool write = pos >= 0 && gf < e.n_feat;
+    const bool rope = is_k && e.rope_cos != nullptr;
+    for (int j0 = 0; j0 < half; j0 += 8) {
+      float x[8], y[8];   // features j0.. and their partners half + j0..
+      tmem_ld8(t_lane + h0 + j0, x);
+      tmem_ld8(t_lane + h0 + half + j0, y);
+      float4 cv[2], sv[2];
+      if (rope && write) {
+        const float4* cp = reinterpret_cast<const float4*>(e.rope_cos + static_cast<size_t>(pos) * half + j0);
+        const float4* sp = reinterpret_cast<const float4*>(e.rope_sin + static_cast<size_t>(pos) * half + j0);
+        cv[0] = __ldg(cp); cv[1] = __ldg(cp + 1);
+        sv[0] = __ldg(sp); sv[1] = __ldg(sp + 1);
+      }
+      tmem_ld_wait();
+      if (!write) continue;
+      if (rope) {
+        const float c[8] = {cv[0].x, cv[0].y, cv[0].z, cv[0].w, cv[1].x, cv[1].y, cv[1].z, cv[1].w};
+        const float sn[8] = {sv[0].x, sv[0].y, sv[0].z, sv[0].w, sv[1].x, sv[1].y, sv[1].z, sv[1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float a = x[i], b = y[i];
+          x[i] = a * c[i] - b * sn[i];   // rotate-half: (d, d + Dh/2) pairs
+          y[i] = b * c[i] + a * sn[i];
+        }
+      }
+      store8(dst, e.out_bf16, row * Dh + j0, x);
+      store8(dst, e.out_bf16, row * Dh + half + j0, y);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace dfl
 
@@ -429,7 +579,7 @@ static_assert(sizeof(SmemHeader) + 1023 <= kSmemHeaderBytes, "shared-memory head
 // Tile (m_tile, n_tile) of grid index t. Decode orientation (A = weights):
 // n_tile fastest, so the CTAs that share a weight tile are adjacent in launch
 // order and read it from HBM once. Token-major orientation (B = weights):
-// groups of group_m token tiles, m fastest inside a group, so the CTAs of a
+// groups of group_m (16) token tiles, m fastest inside a group, so the CTAs of a
 // wave share a few token tiles and a band of weight tiles instead of
 // re-streaming either operand for every tile of the other.
 __device__ __forceinline__ void tile_of(const GemmArgs& g, int t, int& m, int& n) {
@@ -614,7 +764,9 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
     if (etid == 0) hdr->epi_ok = *reinterpret_cast<volatile int*>(&hdr->abort_flag) == 0 ? 1 : 0;
     named_bar(1, 128);
     const bool ok = hdr->epi_ok != 0;
-    if (ok) {
+    if (ok && token_major_direct<kOp>() && !g.swap && g.splits == 1 && g.epi.ss_in == nullptr) {
+      epilogue_token_major<kOp>(g, t_lane, m_tile * kBM + row, n_tile);
+    } else if (ok) {
       const int n_chunks = (g.bn + kBM - 1) / kBM;
       if (g.splits == 1) {
         for (int c = 0; c < n_chunks; ++c) {
@@ -792,7 +944,7 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   p.m_tiles = m_tiles;
   p.group_m = 0;
   if (!weights_a) {
-    p.group_m = 8;
+    p.group_m = 16;
     if (const char* e = getenv("DFLASH_GEMM_GROUP_M")) p.group_m = atoi(e);   // tuning override
   }
   p.b_split = b_split ? 1 : 0;
