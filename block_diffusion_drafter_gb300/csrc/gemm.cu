@@ -160,6 +160,50 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
                            ? gain_at(e.xg_gain, e.xg_bf16, m_tile * kBM + etid)
                            : 0.f;
       constexpr int kB = epi_batch<kOp, kWide>();
+      if constexpr (kOp == EPI_ADD_F32 && kWide) {
+        // (wide residual-add tiles are decode tiles: weights along A rows)
+        // Wide tiles: this thread's feature is fixed (a = etid); its tokens
+        // come in batches of 16 whose residual loads are all issued first.
+        const int a = etid, feat = m_tile * kBM + a;
+        const bool fok = feat < e.n_feat;
+        constexpr int NB = 16;
+        float* h = reinterpret_cast<float*>(e.out);
+        for (int b0 = 0; b0 < cols; b0 += NB) {
+          float v[NB], r[NB];
+#pragma unroll
+          for (int u = 0; u < NB; ++u) {
+            const int b = b0 + u, tok = n_tile * g.bn + col0 + b;
+            const bool ok = fok && b < cols && tok < e.n_tok;
+            v[u] = ok ? S[b * kSLD + a] : 0.f;
+            if (ok && e.ss_in != nullptr) v[u] *= rstd[b];
+            r[u] = ok ? h[static_cast<size_t>(tok) * e.ld + feat] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < NB; ++u) {
+            const int b = b0 + u, tok = n_tile * g.bn + col0 + b;
+            if (!(fok && b < cols && tok < e.n_tok)) continue;
+            const float hn = r[u] + v[u];
+            h[static_cast<size_t>(tok) * e.ld + feat] = hn;
+            if (e.xg_out != nullptr) {
+              int row = tok;
+              if (e.xg_mask_rows) {
+                const int i = tok % e.rows_per_seq;
+                row = i == 0 ? -1 : (tok / e.rows_per_seq) * e.gamma + i - 1;
+              }
+              if (row >= 0) {
+                const size_t xi = static_cast<size_t>(row) * e.d_model + feat;
+                const float xv = gx * hn;
+                if (e.xg_bf16)
+                  store_hilo(reinterpret_cast<__nv_bfloat16*>(e.xg_out), xi, e.lo_off, xv);
+                else
+                  reinterpret_cast<float*>(e.xg_out)[xi] = xv;
+              }
+              const_cast<float*>(S)[b * kSLD + a] = hn * hn;
+            }
+          }
+        }
+      }
+      if constexpr (!(kOp == EPI_ADD_F32 && kWide))
       for (int base = etid; base < total; base += 128 * kB) {
         float v[kB], r[kB];
         size_t o[kB];
@@ -281,6 +325,67 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
       const int Dh = e.head_dim, half = Dh >> 1;
       const int nq = e.n_q_heads * Dh, nk = e.n_kv_heads * Dh;
       constexpr int kB = epi_batch<kOp, kWide>();
+      if constexpr (kWide) {
+        // Wide tiles (decode tiles: weights along A rows; a token-major
+        // injection takes the direct epilogue): this thread's output feature, its kind (q, k or v),
+        // head, RoPE partner row and table column are fixed; its tokens come
+        // in batches of 8 whose table loads are all issued first.
+        const int a = etid, gf = m_tile * kBM + a;
+        int f = gf, layer = e.layer;
+        if (kOp == EPI_KV) {
+          layer = gf / e.feat_per_layer;
+          f = gf - layer * e.feat_per_layer + nq;   // position within the [Q; K; V] rows
+        }
+        const bool fok = gf < e.n_feat;
+        const int d = f % Dh, j = d < half ? d : d - half;
+        const int kind = f < nq ? 1 : (f < nq + nk ? 2 : 3);
+        const int head = kind == 2 ? (f - nq) / Dh : (f - nq - nk) / Dh;
+        const int pa = d < half ? a + half : a - half;   // partner row, same head (in range: 128 % Dh == 0)
+        const bool rope = kind != 3 && e.rope_cos != nullptr;
+        void* dst = kind == 1 ? e.out : (kind == 2 ? e.k_cache : e.v_cache);
+        constexpr int NB = 8;
+        for (int b0 = 0; b0 < cols; b0 += NB) {
+          float y[NB], p[NB], c[NB], sn[NB];
+          int pp[NB];
+          bool ok[NB];
+#pragma unroll
+          for (int u = 0; u < NB; ++u) {
+            const int b = b0 + u, tok = n_tile * g.bn + col0 + b;
+            const int pos = b < cols ? ti->pos[b] : -1;
+            ok[u] = fok && b < cols && (kind == 1 ? tok < e.n_tok : pos >= 0);
+            pp[u] = pos < 0 ? 0 : pos;
+            y[u] = ok[u] ? S[b * kSLD + a] : 0.f;
+            p[u] = ok[u] && rope ? S[b * kSLD + pa] : 0.f;
+            c[u] = 1.f;
+            sn[u] = 0.f;
+            if (ok[u] && rope) {
+              const size_t t = static_cast<size_t>(pp[u]) * half + j;
+              c[u] = e.rope_cos[t];
+              sn[u] = e.rope_sin[t];
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < NB; ++u) {
+            if (!ok[u]) continue;
+            const int b = b0 + u, tok = n_tile * g.bn + col0 + b;
+            float val = y[u];
+            if (rope) val = d < half ? y[u] * c[u] - p[u] * sn[u] : y[u] * c[u] + p[u] * sn[u];
+            if (e.ss_in != nullptr) val *= rstd[b];
+            size_t o;
+            if (kind == 1) {
+              o = static_cast<size_t>(tok) * e.ld + f;
+            } else {
+              const int sq = ti->seq[b];   // the sequence, or for paged caches the row's page
+              o = e.page_table != nullptr
+                      ? (((static_cast<size_t>(layer) * e.n_pages + sq) * e.n_kv_heads + head) * kPageKeys +
+                         pp[u] % kPageKeys) * Dh + d
+                      : (((static_cast<size_t>(layer) * e.max_batch + sq) * e.n_kv_heads + head) * e.ncap + pp[u]) *
+                                Dh + d;
+            }
+            store_out(dst, e.out_bf16, o, val);
+          }
+        }
+      } else {
       for (int base = etid; base < total; base += 128 * kB) {
         float y[kB], cs[kB];  // value and its RoPE partner
         size_t o[kB];
@@ -365,6 +470,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
           void* dst = kind[u] == 1 ? e.out : (kind[u] == 2 ? e.k_cache : e.v_cache);
           store_out(dst, e.out_bf16, o[u], val);
         }
+      }
       }
       break;
     }

@@ -63,10 +63,16 @@ def oracle_context(gd, taps_b):
     return [k for k, _ in kv], [v for _, v in kv]
 
 
-@pytest.mark.parametrize("wl", [SMALL, synth.WORKLOADS["tiny_f32_L1_N128"].replace(batch=2)],
-                         ids=["bf16_tcgen05", "fp32_simt"])
+LENS = {3: [300, 45, 0], 2: [200, 9], 5: [60, 33, 0, 17, 50]}
+
+
+# batch 5: 300 injected rows and 85 block rows, so that injection and the
+# block's Q/K/V projection take the decode GEMM's wide-tile epilogues
+@pytest.mark.parametrize("wl", [SMALL, SMALL.replace(batch=5, ctx=60),
+                                synth.WORKLOADS["tiny_f32_L1_N128"].replace(batch=2)],
+                         ids=["bf16_tcgen05", "bf16_wide_tiles", "fp32_simt"])
 def test_paged_cache_matches_the_oracle_and_the_contiguous_cache(dfl, wl):
-    lens = [300, 45, 0][: wl.batch] if wl.batch == 3 else [200, 9]
+    lens = LENS[wl.batch]
     cap = 512
     gd = H.GpuDrafter(dfl, wl, max_rows=max(sum(lens), 16), ctx_capacity=cap)
     B = wl.batch
