@@ -88,6 +88,8 @@ _SIGS = {
     "dflash_rope_tables": (_I, [ctypes.POINTER(Config), _I, _P, _P]),
     "dflash_linear": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "dflash_verify_accept_noalloc": (_I, [ctypes.POINTER(Config), _P, _I, _P, _I, _P, _P, _P, _P]),
+    "dflash_attention": (_I, [ctypes.POINTER(Config), _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ,
+                              ctypes.POINTER(Trace), _P]),
     "dflash_draft_block_dyn": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _P,
                                     _I, _I, _P, _P, _P, _P, _P, _P, _SZ, ctypes.POINTER(Trace), _P]),
     "dflash_verify_accept_dyn": (_I, [ctypes.POINTER(Config), _P, _I, _P, _P, _I, _P, _P, _P, _P, _SZ,
@@ -378,6 +380,17 @@ def dflash_verify_accept_noalloc(cfg, target_logits, draft, tau, committed, next
     _check("dflash_verify_accept_noalloc", load().dflash_verify_accept_noalloc(
         ctypes.byref(cfg), _ptr(target_logits), dt, _ptr(draft), B, _ptr(tau), _ptr(committed),
         _ptr(next_anchor), _stream(stream)))
+
+
+def dflash_attention(cfg, q, ctx_len, max_ctx_hint, layer, k_cache, v_cache, out, dev_status,
+                     ws: Workspace, trace=None, stream=None):
+    """One layer's context attention (the drafting pass's attention step):
+    q, out [B*R, Hq*Dh]; the block's K/V already in cache rows ctx_len.."""
+    B = ctx_len.shape[0]
+    _check("dflash_attention", load().dflash_attention(
+        ctypes.byref(cfg), _ptr(q), _ptr(ctx_len), B, int(max_ctx_hint), int(layer), _ptr(k_cache),
+        _ptr(v_cache), _ptr(out), _ptr(dev_status), ws.ptr, ws.nbytes,
+        ctypes.byref(trace) if trace is not None else None, _stream(stream)))
 
 
 def dflash_linear(x, w, y, ws: Workspace, stream=None):

@@ -110,6 +110,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int G = p.n_q_heads / p.n_kv_heads;
   const int n_q = G * p.R;
 
+  // The first tiles of this split's context K/V do not depend on the kernel
+  // this one waits for: ask L2 for them now, so that the HBM reads overlap
+  // that kernel's tail and this kernel's set-up (a hint only: the TMA loads
+  // below read whatever the memory holds after the wait). Rows stay inside
+  // this (layer, sequence, KV head) slab of the cache.
+  if (threadIdx.x == 64 && p.page_table == nullptr) {
+    const int kb0 = sp * p.chunk;
+    const size_t slab0 = (static_cast<size_t>(p.layer) * p.max_batch + b) * p.n_kv_heads + kvh;
+    for (int t = 0; t < p.prefetch_tiles; ++t) {
+      const int r0 = kb0 + t * kTileKeys, r1 = min(r0 + kTileKeys, p.ncap);
+      if (r0 >= r1) break;
+      const size_t off = (slab0 * p.ncap + r0) * DH;
+      const uint32_t bytes = static_cast<uint32_t>(r1 - r0) * DH * 2;
+      prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(p.k_cache) + off, bytes);
+      prefetch_l2_bulk(reinterpret_cast<const __nv_bfloat16*>(p.v_cache) + off, bytes);
+    }
+  }
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&hdr->k_full[i]), 1);
@@ -623,7 +641,20 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs p) {
 
 namespace dfl {
 
-cudaError_t launch_attention_tc(const AttnArgs& a, cudaStream_t stream, bool pdl) {
+cudaError_t launch_attention_tc(const AttnArgs& a_in, cudaStream_t stream, bool pdl) {
+  AttnArgs a = a_in;
+  // K/V tiles per split asked of L2 before the dependency wait: off by
+  // default. Measured at 32768 keys: attention calls back to back in a graph
+  // 28.3 -> 27.3 us with 3 tiles, but inside the drafting step, where the
+  // QKV projection before it streams weights at the HBM peak, no gain (C3
+  // step 835 vs 840 us). DFLASH_ATTN_PREFETCH sets the count (tuning).
+  static int prefetch = -1;
+  if (prefetch < 0) {
+    const char* e = getenv("DFLASH_ATTN_PREFETCH");
+    prefetch = e != nullptr ? atoi(e) : 0;
+    if (prefetch < 0) prefetch = 0;
+  }
+  a.prefetch_tiles = prefetch;
   if (a.head_dim != 64 && a.head_dim != 128) return cudaErrorInvalidValue;
   if ((a.n_q_heads / a.n_kv_heads) * a.R > 128) return cudaErrorInvalidValue;
   const bool global = a.splits > 1 && a.merge_global;

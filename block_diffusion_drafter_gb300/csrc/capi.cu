@@ -887,6 +887,50 @@ dflash_status dflash_verify_sample(const dflash_config* c, const void* target_lo
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
+dflash_status dflash_attention(const dflash_config* c, const void* q, const int32_t* ctx_len, int B,
+                               int max_ctx_hint, int layer, const void* k_cache, const void* v_cache,
+                               void* out, int32_t* dev_status, void* ws, size_t ws_bytes,
+                               dflash_trace* trace, dflash_stream_t stream) {
+  dflash_status st = dflash_check_config(c);
+  if (st != DFLASH_OK) return st;
+  if (B < 1 || B > c->max_batch || max_ctx_hint < 0 || layer < 0 || layer >= c->n_layers || q == nullptr ||
+      ctx_len == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr || dev_status == nullptr ||
+      !trace_ok(trace))
+    return DFLASH_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(c);
+  if (ws == nullptr || ws_bytes < L.fixed) return DFLASH_ERR_WORKSPACE;
+  if ((st = check_arch()) != DFLASH_OK) return st;
+  const int R = c->gamma + 1, es = elem_bytes(c);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.layer = layer;
+  a.n_layers = c->n_layers;
+  a.ctx_len = ctx_len;
+  a.out = out;
+  a.dev_status = dev_status;
+  a.B = B; a.R = R; a.n_q_heads = c->n_q_heads; a.n_kv_heads = c->n_kv_heads;
+  a.head_dim = c->head_dim; a.ncap = c->ctx_capacity; a.max_batch = c->max_batch;
+  a.bf16 = c->dtype == DFLASH_BF16;
+  plan_attention(B, R, c->n_q_heads, c->n_kv_heads, c->head_dim, max_ctx_hint, c->ctx_capacity,
+                 num_sms_of_current_device(), &a.splits, &a.chunk, &a.merge_global);
+  a.partials = at<float>(ws, L.attn_part);
+  Tracer tr{trace, s};
+  const double kvb = 2.0 * B * c->n_kv_heads * static_cast<double>(max_ctx_hint + R) * c->head_dim * es;
+  const double fl = 4.0 * B * c->n_q_heads * R * static_cast<double>(max_ctx_hint + R) * c->head_dim;
+  tr.before(DFLASH_K_ATTN, kvb + 2.0 * B * R * c->n_q_heads * c->head_dim * es, fl);
+  cudaError_t e = launch_attention(a, s, use_pdl());
+  tr.after();
+  if (e == cudaSuccess && a.bf16 && a.splits > 1 && a.merge_global) {
+    tr.before(DFLASH_K_ATTN, 0.0, 0.0);
+    e = launch_attention_merge(a, s, use_pdl());
+    tr.after();
+  }
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
 static dflash_status verify_accept_impl(const dflash_config* c, const void* target_logits,
                                         dflash_dtype logits_dtype, const int32_t* draft,
                                         const int32_t* gamma_b, int B, int32_t* tau,

@@ -151,6 +151,7 @@ struct AttnArgs {
   int bf16;
   const int32_t* page_table;   // NULL, or paged caches as in Epi
   int n_pages, pages_per_seq;
+  int prefetch_tiles;          // K/V tiles per split asked of L2 before the dependency wait
 };
 // Floats of one split's partial result: 128 unnormalised O rows of head_dim,
 // then (running max, row sum) of each row.

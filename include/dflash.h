@@ -404,6 +404,24 @@ dflash_status dflash_rope_tables(const dflash_config* cfg, int n_pos,
 dflash_status dflash_linear(dflash_dtype dtype, const void* x, const void* w, float* y, int M,
                             int N, int K, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
+/* Context attention of one drafter layer on its own: the attention step of
+ * dflash_draft_block ([P1] "KV Injection 메커니즘", [P4] §3.2), exposed as a
+ * building block like dflash_linear (tests, timing of the split-KV kernels):
+ *   out[b*R + i, h] = softmax(q[b*R + i, h] . K^T / sqrt(Dh)) V
+ * over keys 0 .. ctx_len[b] + gamma of layer `layer`, sequence b and KV head
+ * h / (Hq/Hkv) -- the injected context followed by the block's own R rows,
+ * which must already be in cache rows ctx_len[b] .. ctx_len[b] + gamma
+ * (where dflash_draft_block writes them). No mask, no RoPE (q and the cached
+ * K are used as given).
+ * q, out: device [B*R, Hq*Dh] of cfg.dtype; ctx_len: device [B];
+ * k_cache, v_cache: [L, max_batch, Hkv, Ncap, Dh]; max_ctx_hint as in
+ * dflash_draft_block; 0 <= layer < L. The workspace holds the split partials
+ * of long contexts. */
+dflash_status dflash_attention(const dflash_config* cfg, const void* q, const int32_t* ctx_len, int B,
+                               int max_ctx_hint, int layer, const void* k_cache, const void* v_cache,
+                               void* out, int32_t* dev_status, void* ws, size_t ws_bytes,
+                               dflash_trace* trace, dflash_stream_t stream);
+
 /* Greedy verification without a workspace, for callers that cannot allocate
  * device memory: a serving engine whose memory pool already owns the GPU's
  * memory, a plugin running inside another runtime's step, or a hot loop in
