@@ -115,6 +115,11 @@ void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap
   } else {
     sp = (2 * sms + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
     if (sp > kMaxAttnCluster) sp = kMaxAttnCluster;
+    // The kernel holds one CTA per SM: when the (sequence, KV head) pairs
+    // times the splits exceed one wave and one wave still gives every pair
+    // two splits or more, take one wave (equal-length contexts finish
+    // together; a third wave of a few CTAs would cost a whole split's time)
+    if (per_seq * sp > sms && sms / per_seq >= 2) sp = sms / per_seq;
   }
   // whole 128-key tiles per split (the tcgen05 kernel's tile)
   c = ((n_keys + sp - 1) / sp + 127) / 128 * 128;
