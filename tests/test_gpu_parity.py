@@ -26,7 +26,10 @@ def dfl(lib):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (17, 384, 256), (100, 256, 4096),
                                    (272, 640, 512), (600, 384, 1024), (2048, 1024, 512),
-                                   (33, 4096, 4096)])
+                                   (33, 4096, 4096),
+                                   # token-major tiles whose feature count is not a multiple of
+                                   # 16 (scalar stores) or of the 256-feature tile (a ragged last tile)
+                                   (700, 200, 256), (1030, 600, 320)])
 def test_linear_matches_fp32_matmul(dfl, dtype, M, N, K):
     g = torch.Generator(device="cuda").manual_seed(M * 7919 + N * 31 + K)
     x = torch.randn((M, K), generator=g, device="cuda").to(dtype)
@@ -141,6 +144,16 @@ def test_chain_small_bf16_ragged_batch(dfl):
 def test_chain_small_bf16_long_prefill_plain_gemm(dfl):
     # > 512 fused rows: context fusion / injection take the token-major GEMM
     run_chain(dfl, SMALL.replace(batch=2, ctx=700), [700, 513])
+
+
+def test_chain_bf16_d384_prefill_half_valid_feature_tile(dfl):
+    # D = 384: the token-major fusion tiles are 256 features wide, so the
+    # second tile has 128 valid features (its sums of squares and stores
+    # must stop at D); Dh = 64 heads: four per 256-feature injection tile
+    wl = synth.Workload("d384_bf16", n_layers=1, d_target=128, n_taps=5, d_model=384, n_q_heads=6,
+                        n_kv_heads=2, head_dim=64, d_ffn=512, vocab=1003, gamma=16, dtype="bf16",
+                        batch=2, ctx=600, seed=13)
+    run_chain(dfl, wl, [600, 77])
 
 
 def test_chain_small_bf16_rope_off(dfl):
