@@ -641,6 +641,24 @@ def measure_workload(dfl, wl: synth.Workload, dev, steps: int, peak_gbs: float) 
     return r
 
 
+def oracle_step_ms(wl_name: str, steps: int, threads: int | None) -> float:
+    """ms per drafting cycle of the oracle on the host for a small workload, in a
+    child process whose BLAS runs on `threads` threads (None: all cores)."""
+    code = ("import sys, time, json; sys.path.insert(0, %r); import synth, bench\n"
+            "wl = synth.WORKLOADS[%r]; oc = bench.OracleCycle(wl, synth.weights(wl, 'cpu'), 'cpu')\n"
+            "oc.step(); t0 = time.perf_counter()\n"
+            "for _ in range(%d): oc.step()\n"
+            "print(json.dumps((time.perf_counter() - t0) * 1e3 / %d))") % (ROOT, wl_name, steps, steps)
+    env = dict(os.environ)
+    if threads is not None:
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k] = str(threads)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=300)
+    if out.returncode != 0:
+        return float("nan")
+    return float(out.stdout.strip().splitlines()[-1])
+
+
 class OracleCycle:
     """The CPU oracle running the same drafting cycle (float64 numpy)."""
 
@@ -862,6 +880,12 @@ def run_gpu(args):
         for name in ("tiny_f32_L1_N128", "qwen3_8b_L5_N32768_B1", "qwen3_8b_L5_ragged_B16"):
             if name != wl.name:
                 extra[name] = measure_workload(dfl, synth.WORKLOADS[name], dev, min(args.steps, 20), hbm)
+        # the tiny workload's oracle cycle on the host, one thread and all cores
+        if "tiny_f32_L1_N128" in extra:
+            extra["tiny_f32_L1_N128"]["oracle_ms_per_step_1_thread"] = round(
+                oracle_step_ms("tiny_f32_L1_N128", 20, 1), 3)
+            extra["tiny_f32_L1_N128"]["oracle_ms_per_step_all_cores"] = round(
+                oracle_step_ms("tiny_f32_L1_N128", 20, None), 3)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:

@@ -88,6 +88,7 @@ _SIGS = {
     "dflash_rope_tables": (_I, [ctypes.POINTER(Config), _I, _P, _P]),
     "dflash_linear": (_I, [_I, _P, _P, _P, _I, _I, _I, _P, _SZ, _P]),
     "dflash_verify_accept_noalloc": (_I, [ctypes.POINTER(Config), _P, _I, _P, _I, _P, _P, _P, _P]),
+    "dflash_selftest_wait_timeout": (_I, [_P, _P]),
     "dflash_attention": (_I, [ctypes.POINTER(Config), _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ,
                               ctypes.POINTER(Trace), _P]),
     "dflash_draft_block_dyn": (_I, [ctypes.POINTER(Config), ctypes.POINTER(WeightsStruct), _P, _P, _P,
@@ -391,6 +392,11 @@ def dflash_attention(cfg, q, ctx_len, max_ctx_hint, layer, k_cache, v_cache, out
         ctypes.byref(cfg), _ptr(q), _ptr(ctx_len), B, int(max_ctx_hint), int(layer), _ptr(k_cache),
         _ptr(v_cache), _ptr(out), _ptr(dev_status), ws.ptr, ws.nbytes,
         ctypes.byref(trace) if trace is not None else None, _stream(stream)))
+
+
+def dflash_selftest_wait_timeout(dev_status, stream=None):
+    """Launches the bounded-wait self-test: dev_status reads ERR_TIMEOUT after ~1 s."""
+    _check("dflash_selftest_wait_timeout", load().dflash_selftest_wait_timeout(_ptr(dev_status), _stream(stream)))
 
 
 def dflash_linear(x, w, y, ws: Workspace, stream=None):

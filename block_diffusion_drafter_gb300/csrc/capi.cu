@@ -203,6 +203,15 @@ size_t dflash_workspace_bytes(const dflash_config* c, int max_rows) {
   return L.fixed + align256(static_cast<size_t>(max_rows) * row_ss_bytes_per_row(c));
 }
 
+dflash_status dflash_selftest_wait_timeout(int32_t* dev_status, dflash_stream_t stream) {
+  if (dev_status == nullptr) return DFLASH_ERR_INVALID_ARG;
+  dflash_status st = check_arch();
+  if (st != DFLASH_OK) return st;
+  return launch_wait_selftest(dev_status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DFLASH_OK
+             : DFLASH_ERR_CUDA;
+}
+
 dflash_status dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream) {
   if (ws == nullptr || ws_bytes == 0) return DFLASH_ERR_INVALID_ARG;
   if (cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

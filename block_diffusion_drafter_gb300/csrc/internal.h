@@ -222,6 +222,8 @@ cudaError_t launch_verify(const void* logits, int bf16, const int32_t* draft, co
                           int32_t* next_anchor, unsigned long long* keys, int* counters,
                           cudaStream_t s, bool pdl);
 cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t s, bool pdl);
+// One CTA whose bounded wait on an mbarrier nothing arrives on runs out.
+cudaError_t launch_wait_selftest(int* dev_status, cudaStream_t s);
 
 int num_sms_of_current_device();
 // DFLASH_ERR_ARCH unless the current device is sm_103 (cached per device).

@@ -191,6 +191,19 @@ __global__ void kv_advance_kernel(int32_t* ctx_len, const int32_t* n_new, int B,
   ctx_len[b] += nn;
 }
 
+// Failure-detection self-test: one thread waits on an mbarrier that nothing
+// arrives on, through the bounded wait every kernel of the library uses
+// (about 1 s of SM clock), then reports DFLASH_ERR_TIMEOUT. No asynchronous
+// copy or tensor-core work is in flight, so the CTA exits cleanly and the
+// context stays usable.
+__global__ void wait_selftest_kernel(int* dev_status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait(smem_u32(&bar), 0)) report(dev_status, DFLASH_ERR_TIMEOUT);
+}
+
 __global__ void copy_f32_kernel(float* dst, const float* src, size_t n) {
   pdl_launch_dependents();
   pdl_wait();
@@ -331,6 +344,10 @@ cudaError_t launch_kv_advance(int32_t* ctx_len, const int32_t* n_new, int B, int
                               int reserve, int* dev_status, cudaStream_t s, bool pdl) {
   return launch_ex(kv_advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s, pdl, ctx_len, n_new, B,
                    Tmax, ncap, reserve, dev_status);
+}
+
+cudaError_t launch_wait_selftest(int* dev_status, cudaStream_t s) {
+  return launch_ex(wait_selftest_kernel, dim3(1), dim3(32), 0, s, false, dev_status);
 }
 
 cudaError_t launch_copy_f32(float* dst, const float* src, size_t n, cudaStream_t s, bool pdl) {

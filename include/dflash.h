@@ -177,6 +177,15 @@ size_t dflash_kv_cache_bytes(const dflash_config* cfg);
  * cfg.max_batch sequences per draft / verify call. 0 on a bad cfg. */
 size_t dflash_workspace_bytes(const dflash_config* cfg, int max_rows);
 
+/* Failure-detection self-test. Every kernel of this library bounds its waits
+ * on mbarriers (about 1 s of SM clock, 2e9 cycles) and, when one runs out,
+ * writes DFLASH_ERR_TIMEOUT to the status word and exits instead of hanging.
+ * This call launches one CTA whose wait, through the same bounded-wait
+ * routine, has nothing to wait for: after about a second dev_status (device
+ * int32, 0 before the call) holds DFLASH_ERR_TIMEOUT and the context is still
+ * usable. Asynchronous on `stream`. */
+dflash_status dflash_selftest_wait_timeout(int32_t* dev_status, dflash_stream_t stream);
+
 /* Zeroes a workspace once after allocation (its tile counters must start at
  * zero; every kernel leaves them at zero again). Asynchronous on stream. */
 dflash_status dflash_workspace_init(void* ws, size_t ws_bytes,
