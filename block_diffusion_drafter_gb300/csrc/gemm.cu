@@ -702,6 +702,46 @@ __device__ __forceinline__ void tile_of(const GemmArgs& g, int t, int& m, int& n
   n = r / gm;
 }
 
+// Split-K reduction of this CTA's token columns [cb, cb + cols) of a tile:
+// the fp32 partials of the kS splits ([col][row] in each cluster CTA's shared
+// memory) summed in ascending split order into S. A thread takes items of 4
+// rows of one column; kG = 8 / kS items' remote loads of all splits are
+// requested before any is added, so a slice of many columns costs a few
+// distributed-shared-memory round trips rather than one per item.
+template <int kS>
+__device__ __forceinline__ void reduce_split_slice(float* S, uint32_t p_local, int cb, int cols, int etid) {
+  constexpr int kG = kMaxSplitK / kS > 0 ? kMaxSplitK / kS : 1;
+  const int n_items = cols * (kBM / 4);
+  for (int it0 = etid; it0 < n_items; it0 += 128 * kG) {
+    float4 v[kG][kS];
+#pragma unroll
+    for (int gi = 0; gi < kG; ++gi) {
+      const int it = it0 + gi * 128;
+      const int b = it / (kBM / 4), a = (it % (kBM / 4)) * 4;
+      const uint32_t off = static_cast<uint32_t>(((cb + b) * kBM + a) * 4);
+#pragma unroll
+      for (int sp = 0; sp < kS; ++sp)
+        v[gi][sp] = it < n_items ? ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(sp)))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int gi = 0; gi < kG; ++gi) {
+      const int it = it0 + gi * 128;
+      if (it >= n_items) break;
+      const int b = it / (kBM / 4), a = (it % (kBM / 4)) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kS; ++sp) {
+        acc.x += v[gi][sp].x; acc.y += v[gi][sp].y; acc.z += v[gi][sp].z; acc.w += v[gi][sp].w;
+      }
+      S[b * kSLD + a] = acc.x;
+      S[b * kSLD + a + 1] = acc.y;
+      S[b * kSLD + a + 2] = acc.z;
+      S[b * kSLD + a + 3] = acc.w;
+    }
+  }
+}
+
 // One instantiation per (operand type, split activations, epilogue op), so
 // that each launch runs only the code of its own case.
 template <bool kTF32, bool kSplit, int kOp, bool kWide>
@@ -933,25 +973,14 @@ __global__ void __launch_bounds__(kGemmThreads, 3)
       for (int cb = c0; cb < c1; cb += kBM) {
         const int cols = min(kBM, c1 - cb);
         if (ok) {
-          const int n_items = cols * (kBM / 4);
-          for (int it = etid; it < n_items; it += 128) {
-            const int b = it / (kBM / 4), a = (it % (kBM / 4)) * 4;
-            const uint32_t off = static_cast<uint32_t>(((cb + b) * kBM + a) * 4);
-            float4 v[kMaxSplitK];
-#pragma unroll
-            for (int sp = 0; sp < kMaxSplitK; ++sp)
-              if (sp < g.splits) v[sp] = ld_dsmem_f4(mapa_shared(p_local + off, static_cast<uint32_t>(sp)));
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int sp = 0; sp < kMaxSplitK; ++sp) {
-              if (sp < g.splits) {
-                acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w;
-              }
-            }
-            S[b * kSLD + a] = acc.x;
-            S[b * kSLD + a + 1] = acc.y;
-            S[b * kSLD + a + 2] = acc.z;
-            S[b * kSLD + a + 3] = acc.w;
+          switch (g.splits) {
+            case 2: reduce_split_slice<2>(S, p_local, cb, cols, etid); break;
+            case 3: reduce_split_slice<3>(S, p_local, cb, cols, etid); break;
+            case 4: reduce_split_slice<4>(S, p_local, cb, cols, etid); break;
+            case 5: reduce_split_slice<5>(S, p_local, cb, cols, etid); break;
+            case 6: reduce_split_slice<6>(S, p_local, cb, cols, etid); break;
+            case 7: reduce_split_slice<7>(S, p_local, cb, cols, etid); break;
+            default: reduce_split_slice<8>(S, p_local, cb, cols, etid); break;
           }
         }
         named_bar(1, 128);
