@@ -476,6 +476,27 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
     }
     case EPI_ARGMAX: {
       // swap orientation: A rows are vocabulary entries, B rows tokens.
+      if (e.out == nullptr && !(e.temperature > 0.f)) {
+        // greedy, no logits copy: one thread per token scans the tile's 128
+        // vocabulary entries (S rows of consecutive tokens fall in different
+        // banks); the max of the packed keys is the same whatever the order,
+        // and a token costs no chain of dependent warp shuffles
+        const int nf = min(kBM, e.n_feat - m_tile * kBM);
+        for (int b = etid; b < cols; b += 128) {
+          const int tok = n_tile * g.bn + col0 + b;
+          if (tok >= e.n_tok) continue;
+          const float rs = e.ss_in != nullptr ? rstd[b] : 1.f;
+          const float* srow = S + b * kSLD;
+          unsigned long long best = 0ull;
+#pragma unroll 8
+          for (int a = 0; a < nf; ++a) {
+            const unsigned long long key = argmax_key(srow[a] * rs, static_cast<uint32_t>(m_tile * kBM + a));
+            best = key > best ? key : best;
+          }
+          e.keys[static_cast<size_t>(tok) * e.keys_ld + m_tile] = best;
+        }
+        break;
+      }
       const int w = etid >> 5, lane = etid & 31;
       for (int b = w; b < cols; b += 4) {
         const int tok = n_tile * g.bn + col0 + b;

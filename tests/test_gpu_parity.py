@@ -109,8 +109,12 @@ def run_chain(dfl, wl, ctx_lens, check_dumps=True, max_rows=None):
     v_all = gd.v_cache.clone()
     anchors = synth.anchors(wl)
     draft, logits, dump = gd.draft(anchors, max(ctx_lens), want_logits=True, want_dump=check_dumps)
+    # without a logits copy the LM head's argmax takes its other epilogue
+    # (one thread per token): the same drafts bit for bit
+    draft_nl, _, _ = gd.draft(anchors, max(ctx_lens))
     torch.cuda.synchronize()
     gd.check_status()
+    assert torch.equal(draft_nl, draft)
 
     W = gd.W
     for b in range(B):
