@@ -45,12 +45,12 @@ __device__ __forceinline__ void store_out(void* out, int bf16, size_t idx, float
 // Runs on the 128 epilogue threads (etid 0..127). Every op works in batches
 // of a few elements per thread: all global loads of a batch are issued
 // before any of its stores, so the loads overlap instead of serialising
-// behind possibly-aliasing stores. Narrow tiles (a few tokens) use batches of
-// 2: larger batches cost registers and code, and a drafting step at batch 1
-// ran slower with them (758 vs 754 us with 4, 799 us with 8). Wide tiles
-// (many tokens per thread) give the ops whose elements each wait on a global
-// load -- the residual, the RoPE tables -- batches of 4 (the ragged batch-16
-// step: 3.03 vs 3.12 ms).
+// behind possibly-aliasing stores. The generic loop takes batches of
+// epi_batch() elements: 2 for narrow tiles (a few tokens; larger batches cost
+// registers and code, and a drafting step at batch 1 ran slower with them:
+// 758 vs 754 us with 4, 799 us with 8), 4 for the wide instances. The wide
+// decode instances of the residual add and of QKV/KV, where every thread
+// owns one feature across many tokens, have loops of their own.
 template <int kOp, bool kWide>
 __host__ __device__ constexpr int epi_batch() {
   return kWide && (kOp == EPI_QKV || kOp == EPI_KV || kOp == EPI_ADD_F32) ? 4 : 2;
@@ -162,34 +162,52 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
       constexpr int kB = epi_batch<kOp, kWide>();
       if constexpr (kOp == EPI_ADD_F32 && kWide) {
         // (wide residual-add tiles are decode tiles: weights along A rows)
-        // Wide tiles: this thread's feature is fixed (a = etid); its tokens
-        // come in batches of 16 whose residual loads are all issued first.
+        // This thread's feature is fixed (a = etid). Pass 1 adds the residual
+        // to the staged accumulator in place, with 24 tokens' loads in flight
+        // at a time; pass 2 stores h_new (and g (.) h_new) token by token
+        // from shared memory: a short loop instead of an unrolled batch, whose
+        // code would not stay in the instruction cache.
         const int a = etid, feat = m_tile * kBM + a;
-        const bool fok = feat < e.n_feat;
-        constexpr int NB = 16;
         float* h = reinterpret_cast<float*>(e.out);
-        for (int b0 = 0; b0 < cols; b0 += NB) {
-          float v[NB], r[NB];
-#pragma unroll
-          for (int u = 0; u < NB; ++u) {
-            const int b = b0 + u, tok = n_tile * g.bn + col0 + b;
-            const bool ok = fok && b < cols && tok < e.n_tok;
-            v[u] = ok ? S[b * kSLD + a] : 0.f;
-            if (ok && e.ss_in != nullptr) v[u] *= rstd[b];
-            r[u] = ok ? h[static_cast<size_t>(tok) * e.ld + feat] : 0.f;
+        float* Sw = const_cast<float*>(S);
+        const int tok0 = n_tile * g.bn + col0;
+        const int nb = min(cols, e.n_tok - tok0);   // valid tokens of the chunk
+        if (e.xg_out != nullptr) {
+          // output row of g (.) h_new per token (-1: none), once per chunk
+          for (int x = etid; x < cols; x += 128) {
+            const int tok = tok0 + x;
+            int row = tok < e.n_tok ? tok : -1;
+            if (row >= 0 && e.xg_mask_rows) {
+              const int i = tok % e.rows_per_seq;
+              row = i == 0 ? -1 : (tok / e.rows_per_seq) * e.gamma + i - 1;
+            }
+            ti->pos[x] = row;
           }
+          named_bar(1, 128);
+        }
+        if (feat < e.n_feat) {
+          constexpr int NB = 24;
+          for (int b0 = 0; b0 < nb; b0 += NB) {
+            float r[NB];
 #pragma unroll
-          for (int u = 0; u < NB; ++u) {
-            const int b = b0 + u, tok = n_tile * g.bn + col0 + b;
-            if (!(fok && b < cols && tok < e.n_tok)) continue;
-            const float hn = r[u] + v[u];
-            h[static_cast<size_t>(tok) * e.ld + feat] = hn;
-            if (e.xg_out != nullptr) {
-              int row = tok;
-              if (e.xg_mask_rows) {
-                const int i = tok % e.rows_per_seq;
-                row = i == 0 ? -1 : (tok / e.rows_per_seq) * e.gamma + i - 1;
+            for (int u = 0; u < NB; ++u)
+              r[u] = b0 + u < nb ? h[static_cast<size_t>(tok0 + b0 + u) * e.ld + feat] : 0.f;
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+              const int b = b0 + u;
+              if (b < nb) {
+                float v = Sw[b * kSLD + a];
+                if (e.ss_in != nullptr) v *= rstd[b];
+                Sw[b * kSLD + a] = r[u] + v;
               }
+            }
+          }
+#pragma unroll 2
+          for (int b = 0; b < nb; ++b) {
+            const float hn = Sw[b * kSLD + a];
+            h[static_cast<size_t>(tok0 + b) * e.ld + feat] = hn;
+            if (e.xg_out != nullptr) {
+              const int row = ti->pos[b];
               if (row >= 0) {
                 const size_t xi = static_cast<size_t>(row) * e.d_model + feat;
                 const float xv = gx * hn;
@@ -198,7 +216,7 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
                 else
                   reinterpret_cast<float*>(e.xg_out)[xi] = xv;
               }
-              const_cast<float*>(S)[b * kSLD + a] = hn * hn;
+              Sw[b * kSLD + a] = hn * hn;
             }
           }
         }
@@ -304,19 +322,46 @@ __device__ void apply_epilogue(const GemmArgs& g, const float* S, TokInfo* ti, i
       break;
     }
     case EPI_SWIGLU: {
-      // A rows 0..63: gate features m_tile*64 + a; rows 64..127: matching up rows.
-      for (int idx = etid; idx < cols * 64; idx += 128) {
-        const int a = idx & 63, b = idx >> 6;
-        const int feat = m_tile * 64 + a;
+      // A rows 0..63: gate features m_tile*64 + a; rows 64..127: matching up
+      // rows. Four consecutive features per thread (16 threads per token),
+      // written as one 8-byte (bf16) or 16-byte (fp32) store where aligned.
+      const int f0 = m_tile * 64;
+      const bool vec = (e.ld % 4) == 0 && (e.lo_off % 4) == 0;
+      for (int idx = etid; idx < cols * 16; idx += 128) {
+        const int a0 = (idx & 15) * 4, b = idx >> 4;
         const int tok = n_tile * g.bn + col0 + b;
+        const int feat = f0 + a0;
         if (tok >= e.n_tok || feat >= e.n_feat) continue;
         const float rs = e.ss_in != nullptr ? rstd[b] : 1.f;
-        const float gate = S[b * kSLD + a] * rs, up = S[b * kSLD + a + 64] * rs;
+        float y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float gate = S[b * kSLD + a0 + i] * rs, up = S[b * kSLD + a0 + i + 64] * rs;
+          y[i] = silu_f(gate) * up;
+        }
         const size_t oi = static_cast<size_t>(tok) * e.ld + feat;
-        if (e.out_bf16)
-          store_hilo(reinterpret_cast<__nv_bfloat16*>(e.out), oi, e.lo_off, silu_f(gate) * up);
-        else
-          reinterpret_cast<float*>(e.out)[oi] = silu_f(gate) * up;
+        if (vec && feat + 4 <= e.n_feat) {
+          if (e.out_bf16) {
+            __nv_bfloat16 hi[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              hi[i] = __float2bfloat16_rn(y[i]);
+              lo[i] = __float2bfloat16_rn(y[i] - __bfloat162float(hi[i]));
+            }
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e.out);
+            *reinterpret_cast<uint2*>(o + oi) = *reinterpret_cast<const uint2*>(hi);
+            if (e.lo_off) *reinterpret_cast<uint2*>(o + oi + e.lo_off) = *reinterpret_cast<const uint2*>(lo);
+          } else {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + oi) = make_float4(y[0], y[1], y[2], y[3]);
+          }
+        } else {
+          for (int i = 0; i < 4 && feat + i < e.n_feat; ++i) {
+            if (e.out_bf16)
+              store_hilo(reinterpret_cast<__nv_bfloat16*>(e.out), oi + i, e.lo_off, y[i]);
+            else
+              reinterpret_cast<float*>(e.out)[oi + i] = y[i];
+          }
+        }
       }
       break;
     }
@@ -1138,6 +1183,18 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
     const int tiles = m_tiles * p.n_tiles;
     const int slots = num_sms * ctas_per_sm;
     splits = slots / (tiles > 0 ? tiles : 1);
+    if (tiles > slots) {
+      // More tiles than resident slots: the last, partial wave runs nearly
+      // alone. Split K where that shortens the waves: splits s cost
+      // ceil(tiles * s / slots) waves of 1/s the length, plus a reduction
+      // (taken as 1/8 of a wave per split step above 1).
+      double best = 1e30;
+      for (int s = 1; s <= kMaxSplitK && s <= KT / 4; ++s) {
+        const double waves = static_cast<double>((tiles * s + slots - 1) / slots);
+        const double cost = waves / s * (1.0 + 0.125 * (s - 1));
+        if (cost < best - 1e-9) { best = cost; splits = s; }
+      }
+    }
     if (const char* e = getenv("DFLASH_GEMM_SPLITS")) splits = atoi(e);   // tuning override
     if (splits > KT / 4) splits = KT / 4;
     if (splits > kMaxSplitK) splits = kMaxSplitK;
