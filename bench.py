@@ -186,7 +186,21 @@ class DraftCycle:
         self.committed = self.io_out[B * wl.gamma + B:].view(B, R)
         self.next_anchor = torch.empty(B, dtype=torch.int32, device=device)
         self.max_ctx = int(synth.ctx_lengths(wl).max())
+        # The library's trace counts an attention launch's K/V bytes (and
+        # flops) as if every sequence had the longest context: it knows only
+        # the host hint max_ctx, not the per-sequence lengths on the device.
+        # Each sequence reads its own ctx_b + R keys, so for a ragged batch
+        # the records are rescaled to sum_b (ctx_b + R) keys; the query and
+        # output bytes, 2 B R Hq Dh elements, are not part of the rescaling.
+        self.attn_key_ratio = attention_key_ratio(synth.ctx_lengths(wl), R, self.max_ctx)
+        self.attn_qo_bytes = 2.0 * B * R * wl.n_q_heads * wl.head_dim * (2 if wl.dtype == "bf16" else 4)
         torch.cuda.synchronize()
+
+    def algorithmic(self, kind: int, b: float, fl: float):
+        """(bytes, flops) of one traced launch, attention counted per sequence."""
+        if kind != self.dfl.K_ATTN or b <= 0.0:
+            return b, fl
+        return (b - self.attn_qo_bytes) * self.attn_key_ratio + self.attn_qo_bytes, fl * self.attn_key_ratio
 
     def step_inject(self, trace=None):
         """Fusion and injection of the step's new rows."""
@@ -297,6 +311,13 @@ class DraftCycle:
         return rec.struct.count
 
 
+def attention_key_ratio(ctx_lengths, rows: int, max_ctx_hint: int) -> float:
+    """Keys the attention launches read, sum_b (ctx_b + rows), over the keys
+    the library's trace counts, B (max_ctx_hint + rows)."""
+    keys = np.asarray(ctx_lengths, dtype=np.float64) + rows
+    return float(keys.sum() / (keys.size * (max_ctx_hint + rows)))
+
+
 def time_steps(fn, steps: int, stream) -> float:
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -330,7 +351,7 @@ def measure_variant(cyc: DraftCycle, fn, steps: int, tokens: int, peak_gbs: floa
     rec.reset()
     fn(trace=rec.struct)
     torch.cuda.synchronize()
-    b = sum(r[1] for r in rec.records())
+    b = sum(cyc.algorithmic(r[0], r[1], r[2])[0] for r in rec.records())
     us = 1000.0 * ms / steps
     gbs = b / (us * 1e-6) / 1e9
     return {"us_per_step": round(us, 2), "drafted_tok_s": round(tokens / (us * 1e-6), 1),
@@ -354,6 +375,7 @@ def kernel_roofline(cyc: DraftCycle, peak_gbs: float, step_ms: float, reps: int 
         rec.reset()
         cyc.step(trace=rec.struct)
         for kind, b, fl, ms in rec.records():
+            b, fl = cyc.algorithmic(kind, b, fl)
             a = agg.setdefault(kind, [0.0, 0.0, 0.0, 0])
             a[0] += b
             a[1] += fl
