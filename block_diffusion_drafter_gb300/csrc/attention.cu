@@ -113,7 +113,9 @@ void plan_attention(int B, int R, int Hq, int Hkv, int Dh, int max_ctx, int ncap
   } else if (global) {
     sp = wide;
   } else {
-    sp = (2 * sms + per_seq - 1) / per_seq;   // ~2 CTAs per SM in total
+    int per_sm = 2;   // ~2 CTAs per SM in total
+    if (const char* e = getenv("DFLASH_ATTN_CTAS_PER_SM")) per_sm = atoi(e) > 0 ? atoi(e) : 1;   // tuning override
+    sp = (per_sm * sms + per_seq - 1) / per_seq;
     if (sp > kMaxAttnCluster) sp = kMaxAttnCluster;
     // The kernel holds one CTA per SM: when the (sequence, KV head) pairs
     // times the splits exceed one wave and one wave still gives every pair

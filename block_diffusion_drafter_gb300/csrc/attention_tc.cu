@@ -162,8 +162,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // the block's keys: rows 0..gamma_b[b] (clamped to the block), else all R
   const int r_b = p.gamma_b == nullptr ? p.R : min(max(p.gamma_b[b], 1), p.R - 1) + 1;
   const int n_keys = p.ctx_len[b] + r_b;
-  const int k_begin = sp * p.chunk;
-  const int k_end = (sp == p.splits - 1) ? n_keys : min(n_keys, (sp + 1) * p.chunk);
+  // This sequence's keys are split evenly over the splits (whole 128-key
+  // tiles; p.chunk is the split of the longest context). In a ragged batch a
+  // short context then has short splits, instead of its first splits taking
+  // all of it while the rest idle in the cluster until its merge.
+  const int chunk_b = ((n_keys + p.splits - 1) / p.splits + kTileKeys - 1) / kTileKeys * kTileKeys;
+  const int k_begin = sp * chunk_b;
+  const int k_end = (sp == p.splits - 1) ? n_keys : min(n_keys, (sp + 1) * chunk_b);
   const int nt = k_end > k_begin ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
   const int slab = (p.layer * p.max_batch + b) * p.n_kv_heads + kvh;
   volatile int* abort_flag = &hdr->abort_flag;

@@ -142,7 +142,9 @@ struct AttnArgs {
   size_t out_lo_off;      // > 0: bf16 lo = bf16(o - hi) at out + out_lo_off elements
   int* dev_status;
   int B, R, n_q_heads, n_kv_heads, head_dim, ncap, max_batch;
-  int splits, chunk;      // keys per split (multiple of 128); last split takes the rest
+  int splits, chunk;      // keys per split of the longest context (multiple of 128); the
+                          // tcgen05 kernel splits each sequence's own keys evenly (whole
+                          // 128-key tiles); the last split takes the rest
   int merge_global;       // 0: the splits of one (sequence, KV head) form one cluster and merge
                           //    through distributed shared memory;
                           // 1: more splits than a cluster holds: each writes its partial rows
