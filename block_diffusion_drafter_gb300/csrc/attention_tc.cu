@@ -50,6 +50,7 @@ struct AttnSmem {
   uint64_t q_full, s_full[2], s_free[2], p_full, o_done;
   uint32_t tmem_base;
   int abort_flag;
+  int seq;                  // the sequence this CTA's launch slot takes (longest first)
   float pmax[kParts][128];  // per-part row max of the current tile
   float psum[kParts][128];  // per-part row sums at the end
 };
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t q_s = base_s, p_s = q_s + kQBytes, k_s = p_s + kPBytes, v_s = k_s + 2 * kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int sp = blockIdx.x, kvh = blockIdx.y;
+  int b = blockIdx.z;   // until the dependency wait: the launch slot (see below)
   int issued = 0;  // producer lanes: tiles whose TMA loads were issued
   const int G = p.n_q_heads / p.n_kv_heads;
   const int n_q = G * p.R;
@@ -158,6 +160,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = hdr->tmem_base;
   pdl_launch_dependents();
   pdl_wait();
+
+  // Longest contexts first. The (sequence, KV head) clusters start in the
+  // order of their launch slot z = blockIdx.z; in a batch of ragged contexts
+  // slot z takes the sequence of rank z by context length (longest first,
+  // ties by index), so that the longest clusters start first and the short
+  // ones fill in behind them instead of a long one starting last. Equal
+  // contexts keep the identity order.
+  if (p.B > 1 && p.B <= 64) {
+    if (warp == 0) {
+      const int l0 = lane < p.B ? p.ctx_len[lane] : -1;
+      const int l1 = lane + 32 < p.B ? p.ctx_len[lane + 32] : -1;
+      int r0 = 0, r1 = 0;   // ranks of sequences lane and lane + 32
+      for (int m = 0; m < p.B; ++m) {
+        const int lm = __shfl_sync(0xffffffffu, m < 32 ? l0 : l1, m & 31);
+        r0 += (lm > l0 || (lm == l0 && m < lane)) ? 1 : 0;
+        r1 += (lm > l1 || (lm == l1 && m < lane + 32)) ? 1 : 0;
+      }
+      if (lane < p.B && r0 == b) hdr->seq = lane;
+      if (lane + 32 < p.B && r1 == b) hdr->seq = lane + 32;
+    }
+    __syncthreads();
+    b = hdr->seq;
+  }
 
   // the block's keys: rows 0..gamma_b[b] (clamped to the block), else all R
   const int r_b = p.gamma_b == nullptr ? p.R : min(max(p.gamma_b[b], 1), p.R - 1) + 1;
