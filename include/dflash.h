@@ -237,7 +237,10 @@ dflash_status dflash_kv_inject(const dflash_config* cfg, const dflash_weights* w
  *   (not modified). A pass of up to 512 block rows (B * (gamma + 1)) runs as
  *   one projection tile of tokens; larger passes take several 256-row tiles.
  * max_ctx_hint: host upper bound of ctx_len[b] used to size the split-KV grid
- *   (any value is correct; a tight one is faster). Must be >= 0.
+ *   (any value is correct; a tight one is faster). Must be >= 0. The kernel
+ *   divides each sequence's own keys (its device-side ctx_len) among the
+ *   splits; a trace record counts an attention launch's K/V bytes and flops
+ *   as if every sequence had max_ctx_hint keys.
  * k_cache, v_cache: as in dflash_kv_inject. The block's own K/V rows are
  *   written to cache rows ctx_len[b] .. ctx_len[b]+gamma as scratch; those
  *   rows lie beyond ctx_len and carry no context.
