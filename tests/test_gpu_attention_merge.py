@@ -13,8 +13,9 @@ import pytest
 import torch
 
 import synth
+from oracle import dflash_ref as ref
 from tests import harness as H
-from tests.test_gpu_paged import fused_context
+from tests.test_gpu_paged import fused_context, oracle_context
 
 pytestmark = pytest.mark.gpu
 
@@ -31,9 +32,10 @@ def dfl(lib):
     return lib
 
 
-def run(dfl, wl, lens, splits):
+def run(dfl, wl, lens, splits, with_taps=False):
     gd = H.GpuDrafter(dfl, wl, max_rows=max(sum(lens), 16), ctx_capacity=1024)
-    gd.inject(fused_context(gd, lens), lens)
+    h_pad, taps = fused_context(gd, lens, with_taps=True)
+    gd.inject(h_pad, lens)
     old = os.environ.get("DFLASH_ATTN_SPLITS")
     if splits is None:
         os.environ.pop("DFLASH_ATTN_SPLITS", None)
@@ -48,6 +50,8 @@ def run(dfl, wl, lens, splits):
             os.environ.pop("DFLASH_ATTN_SPLITS", None)
         else:
             os.environ["DFLASH_ATTN_SPLITS"] = old
+    if with_taps:
+        return draft, logits, dump, gd, taps
     return draft, logits, dump
 
 
@@ -57,11 +61,20 @@ def test_workspace_merge_equals_cluster_merge(dfl, wl):
     # both plan 128-key splits, 8 of them over the longest context: asked for 8
     # (a cluster holds them) or for 16 (more than a cluster holds: workspace merge)
     d_c, l_c, h_c = run(dfl, wl, lens, 8)
-    d_g, l_g, h_g = run(dfl, wl, lens, 16)
+    d_g, l_g, h_g, gd, taps = run(dfl, wl, lens, 16, with_taps=True)
     assert torch.equal(h_g, h_c)
     assert torch.equal(l_g, l_c)
     assert torch.equal(d_g, d_c)
     assert np.isfinite(l_g.cpu().numpy()).all()
+    # and both against the oracle: ragged contexts, each sequence's keys split
+    # over its own splits, launch slots taken longest context first
+    oc = H.oracle_cfg(wl)
+    anchors = synth.anchors(wl)
+    for b in range(len(lens)):
+        kc, vc = oracle_context(gd, taps[b])
+        out = ref.draft_block(oc, gd.W, int(anchors[b]), kc, vc, lens[b])
+        H.assert_logits_close(l_g[b], out["logits"], f"workspace-merge logits b{b}")
+        H.assert_drafts_match(d_g[b].cpu().numpy(), out["logits"], f"workspace-merge draft b{b}")
 
 
 def test_workspace_merge_with_more_splits_than_lanes_matches_the_oracle(dfl):
