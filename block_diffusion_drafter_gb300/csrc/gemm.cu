@@ -1164,6 +1164,11 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   size_t per_cta = static_cast<size_t>(233472 / target) - 1024;
   if (per_cta > 232448) per_cta = 232448;
   int stages = p.bn <= 128 ? 3 : static_cast<int>((per_cta - kSmemHeaderBytes) / stage);
+  // narrow tiles of 65-128 rows: a 2-stage ring where a third 3-stage CTA
+  // would not fit beside two others (the three CTAs keep as many stages in
+  // flight per SM as two 3-stage ones, and the next kernel's CTAs find room)
+  if (p.bn <= 128 && target == 3)
+    while (stages > 2 && 3 * (kSmemHeaderBytes + static_cast<size_t>(stages) * stage + 1024) > 233472) --stages;
   if (const char* e = getenv("DFLASH_GEMM_STAGES")) stages = atoi(e);   // tuning override
   if (stages > 16) stages = 16;
   if (stages > KT && KT >= 2) stages = KT;
