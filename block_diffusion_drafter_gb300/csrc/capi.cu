@@ -558,15 +558,15 @@ static dflash_status draft_block_impl(const dflash_config* c, const dflash_weigh
   const bool split = bf16 != 0;
   const int rows_max = c->max_batch * R, nmask_max = c->max_batch * c->gamma;
   const int parts = split ? 2 : 1;
-  GemmPlan p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, true, kMaxBN, split);
-  const GemmPlan p_o = plan_gemm(D / kBM, rows, HD, es, cx.sms, true, true, kMaxBN, split);
-  GemmPlan p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, true, kMaxBN, split);
+  GemmPlan p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, true, kMaxBN, split, true);
+  const GemmPlan p_o = plan_gemm(D / kBM, rows, HD, es, cx.sms, true, true, kMaxBN, split, true);
+  GemmPlan p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, true, kMaxBN, split, true);
   if (p_qkv.b_split != p_gu.b_split) {  // both read the same normed activations
-    p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, true, kMaxBN, false);
-    p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, true, kMaxBN, false);
+    p_qkv = plan_gemm(nqkv / kBM, rows, D, es, cx.sms, true, true, kMaxBN, false, true);
+    p_gu = plan_gemm(F / 64, rows, D, es, cx.sms, true, true, kMaxBN, false, true);
   }
-  const GemmPlan p_dn = plan_gemm(D / kBM, rows, F, es, cx.sms, true, true, kMaxBN, split);
-  const GemmPlan p_lm = plan_gemm((V + kBM - 1) / kBM, nmask, D, es, cx.sms, false, true, kMaxBN, split);
+  const GemmPlan p_dn = plan_gemm(D / kBM, rows, F, es, cx.sms, true, true, kMaxBN, split, true);
+  const GemmPlan p_lm = plan_gemm((V + kBM - 1) / kBM, nmask, D, es, cx.sms, false, true, kMaxBN, split, true);
 
   // B boxes bring the valid token rows alone (hi and lo rows when the plan
   // packs split operands) when one box spans the tile

@@ -1116,7 +1116,7 @@ bool make_operand_map(CUtensorMap* map, const void* base, int elem_bytes, uint64
 }
 
 GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
-                   bool weights_a, int bn_cap, bool b_split) {
+                   bool weights_a, int bn_cap, bool b_split, bool chained) {
   GemmPlan p{};
   const int bk = 128 / elem_bytes;
   const int KT = k / bk;
@@ -1164,10 +1164,11 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   size_t per_cta = static_cast<size_t>(233472 / target) - 1024;
   if (per_cta > 232448) per_cta = 232448;
   int stages = p.bn <= 128 ? 3 : static_cast<int>((per_cta - kSmemHeaderBytes) / stage);
-  // narrow tiles of 65-128 rows: a 2-stage ring where a third 3-stage CTA
-  // would not fit beside two others (the three CTAs keep as many stages in
-  // flight per SM as two 3-stage ones, and the next kernel's CTAs find room)
-  if (p.bn <= 128 && target == 3)
+  // narrow tiles of 65-128 rows in a chain of projections: a 2-stage ring
+  // where a third 3-stage CTA would not fit beside two others (the three
+  // CTAs keep as many stages in flight per SM as two 3-stage ones, and the
+  // next projection's CTAs find room as this one's leave)
+  if (chained && p.bn <= 128 && target == 3)
     while (stages > 2 && 3 * (kSmemHeaderBytes + static_cast<size_t>(stages) * stage + 1024) > 233472) --stages;
   if (const char* e = getenv("DFLASH_GEMM_STAGES")) stages = atoi(e);   // tuning override
   if (stages > 16) stages = 16;
@@ -1218,7 +1219,7 @@ GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, 
   // without split-K the epilogue drains 128 columns at a time, and a packed
   // tile must pair each token's hi and lo columns inside one drain
   if (b_split && p.splits == 1 && p.bn > kBM)
-    return plan_gemm(m_tiles, n_rows, k, elem_bytes, num_sms, allow_split, weights_a, bn_cap, false);
+    return plan_gemm(m_tiles, n_rows, k, elem_bytes, num_sms, allow_split, weights_a, bn_cap, false, chained);
   return p;
 }
 

@@ -118,8 +118,10 @@ struct GemmPlan {
 // Chooses tile shape, split count, pipeline depth and grid order for
 // m_tiles A tiles against n_rows B rows over k (elements of elem_bytes each);
 // weights_a: A is the weight matrix (decode orientation), else B is.
+// chained: one of the drafting pass's back-to-back projections (each hands
+// its SMs to the next through programmatic dependent launch).
 GemmPlan plan_gemm(int m_tiles, int n_rows, int k, int elem_bytes, int num_sms, bool allow_split,
-                   bool weights_a, int bn_cap = kMaxBN, bool b_split = false);
+                   bool weights_a, int bn_cap = kMaxBN, bool b_split = false, bool chained = false);
 
 // Builds a 3-D tensor map over a [z][rows][k] row-major operand with a box of
 // (64 or 32 elements of k) x box_rows x 1 and 128-byte swizzle.
