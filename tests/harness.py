@@ -5,11 +5,7 @@ acceptance criteria (written out here so every test applies the same bar).
 Acceptance criteria:
   tau, committed tokens, next anchors   bit-exact
   draft tokens                          equal to the oracle's argmax except
-                                        at near-ties: the oracle's top-2 margin
-                                        < 1e-2, or (given the GPU's logits) a
-                                        flip that the GPU's own logit errors on
-                                        the two tokens explain, each error at
-                                        most 5e-2 * RMS of the row's logits
+                                        where the oracle's top-2 margin < 1e-2
   activations (H_t, KV rows, residual   max |gpu - oracle| <= 3e-2 * RMS(oracle)
   stream after each layer)
   logits                                RMS(gpu - oracle) <= 5e-2 * RMS(oracle)
@@ -25,7 +21,6 @@ from oracle import dflash_ref as ref
 ACT_TOL = 3e-2
 LOGIT_TOL = 5e-2
 MARGIN = 1e-2
-TIE_ERR = 5e-2
 
 
 def oracle_cfg(wl: synth.Workload, rope_theta=None) -> ref.Cfg:
@@ -55,30 +50,13 @@ def assert_logits_close(gpu, want, what="logits", tol=LOGIT_TOL):
 
 
 def assert_drafts_match(gpu_draft, oracle_logits, what="draft", gpu_logits=None):
-    """Bit-exact except at near-ties of the oracle.
-
-    A draft is the argmax of the drafter's logits. A GPU token may differ from
-    the oracle's where the oracle's top-2 margin is below MARGIN, or -- when
-    the GPU's logits are given -- where the GPU's own logits rank its token
-    at least as high as the oracle's, and the GPU's logit errors on the two
-    tokens (each at most TIE_ERR times the RMS of the row's oracle logits,
-    the bound of the per-row logit check) add up to at least the margin:
-    the flip is then the drafter's rounding at a tie, not a wrong token."""
+    """Bit-exact except at near-ties of the oracle (top-2 margin < 1e-2)."""
     d = np.asarray(gpu_draft).reshape(-1)
     lg = np.asarray(oracle_logits, dtype=np.float64).reshape(d.shape[0], -1)
     want = ref.argmax_lowest(lg)
     top2 = np.sort(lg, axis=-1)[:, -2:]
     margin = top2[:, 1] - top2[:, 0]
     bad = (d != want) & (margin >= MARGIN)
-    if gpu_logits is not None and bad.any():
-        gl = ref.f64(gpu_logits).reshape(d.shape[0], -1)
-        for r in np.nonzero(bad)[0]:
-            e_gpu = abs(gl[r, d[r]] - lg[r, d[r]])
-            e_want = abs(gl[r, want[r]] - lg[r, want[r]])
-            bound = TIE_ERR * float(np.sqrt(np.mean(lg[r] * lg[r])))
-            if gl[r, d[r]] >= gl[r, want[r]] and margin[r] <= e_gpu + e_want and max(e_gpu, e_want) <= bound:
-                bad[r] = False
-                report(what, "tokens_excused_by_gpu_logit_error", 1, 0)
     if bad.any():
         rows = np.nonzero(bad)[0]
         detail = []
