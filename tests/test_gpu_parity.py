@@ -203,6 +203,17 @@ def test_chain_small_bf16_batch_32_several_token_tiles(dfl):
     run_chain(dfl, SMALL.replace(n_layers=1, batch=32, ctx=160), lens, check_dumps=True)
 
 
+def test_chain_small_bf16_batch_72_beyond_longest_first_order(dfl):
+    # 72 x 17 = 1224 block rows: every drafting projection takes five 256-row
+    # token tiles; more sequences than the attention's longest-context-first
+    # mapping of launch slots covers (64), so the slots keep launch order;
+    # ragged contexts, some empty, some equal
+    lens = [int(x) for x in np.random.default_rng(72).integers(0, 96, size=72)]
+    lens[5] = 0
+    lens[40] = lens[41]
+    run_chain(dfl, SMALL.replace(n_layers=1, batch=72, ctx=96), lens, check_dumps=False)
+
+
 def test_chain_medium_bf16_batch_40_lm_head_several_tiles(dfl):
     # 40 x 17 = 680 block rows and 640 mask rows: the LM head's token rows
     # span three tiles too; K = 1024..2048 splits the projections over clusters
